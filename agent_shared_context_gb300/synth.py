@@ -1,0 +1,412 @@
+"""Seeded synthetic workloads for the online low-rank KV-cache correction path.
+
+This module only *constructs inputs*: caches, planted cross-agent deltas,
+anchor states and anchor summaries, with the shapes and value distributions of
+the workloads described for KVCMAS ("KVCMAS: Efficient KV cache Correction for
+Shared Context in Multi-Agent Systems", thelatestinai listing of arXiv
+2609.34060: Figure 1 for the PF/PH trajectory structure, Table 3 for the
+per-workload thresholds tau, Table 4 for the ~9K-token vision-language
+trajectories).  It computes none of the method's outputs (no matching, no
+weights, no correction, no score, no factorisation of an observed delta).  Both
+the CUDA library's tests/benchmarks and the fp64 oracle consume the tensors it
+returns; neither side's arithmetic lives here.
+
+Everything is seeded: one ``torch.Generator`` per (workload seed, purpose,
+agent, segment) derived through ``numpy.random.SeedSequence`` so that the data
+of a segment does not depend on how the generation is chunked.  Tensors are
+created on the requested device (CPU for oracle-sized cases, CUDA for the
+full-size workloads); the same seed on a different device gives different (but
+equally distributed) numbers, so a test always generates once and hands the
+same tensors to both sides.
+
+Workloads (names used throughout the tests and the bench):
+
+* ``tiny``      1 layer x 2 KV heads x d=64, fp32, one 256-token shared
+                segment, 2 agents, planted rank-4 delta with singular values
+                (2, 1, 0.5, 0.25) plus N(0, 0.01^2) noise, r=8, 2 anchors,
+                tau=0.3.  Anchor slot 0 is built from the observed delta.
+* ``llama2k``   Llama-3.1-8B KV shape (32 x 8 x 128), bf16, 10 independent
+                requests with one 2,048-token shared segment each, chain of 4
+                agents, geometric delta spectrum (decay 0.85) + N(0, 0.02^2),
+                r=32, 8 anchors, tau=0.32, 10% of segments planted above tau.
+* ``concurrent`` same KV shape, 16 requests, each 16 x (128-token PF + 512-token
+                PH) segments, 8 anchors, tau=0.32.
+* ``longctx``   same KV shape, 1 request, 64 x 512-token PH segments, 16
+                anchors, tau=0.32; slot 0 of every segment is built from the
+                observed delta with oversampling 8 and 2 power iterations.
+* ``vl``        28 x 4 x 128, bf16, one 9,000-token trajectory (17 x 512 +
+                1 x 296 PH segments) whose keys in [1024, 7024) come from 64
+                Gaussian clusters (sigma 0.3), tau=0.6, 20% planted.
+
+``scaled(workload, ...)`` shrinks a workload (layers, heads, requests, segment
+lengths) for oracle-sized parity cases while keeping its structure.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+import torch
+
+__all__ = ["Workload", "WORKLOADS", "workload", "scaled", "EdgeInputs",
+           "WorkloadInputs", "generate", "segment_arrays"]
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    L: int
+    H: int
+    d: int
+    dtype: str                      # "bf16" or "f32"
+    R: int                          # requests held in one cache tensor
+    T: int                          # tokens per request (cache extent)
+    seg_request: Tuple[int, ...]    # PH segment table
+    seg_start: Tuple[int, ...]
+    seg_len: Tuple[int, ...]
+    n_agents: int                   # A0 .. A{n_agents-1}; edges = n_agents - 1
+    A: int                          # anchors per segment (pool slots)
+    r: int                          # retained rank r_Delta
+    tau: float
+    top_k: int = 0                  # 0 -> A
+    temperature: float = 0.1
+    oversample: int = 8
+    power_iters: int = 2
+    energy_frac: float = 0.9
+    delta: str = "geometric"        # "geometric" or "planted"
+    planted_s: Tuple[float, ...] = ()
+    decay: float = 0.85
+    noise: float = 0.02
+    fallback_frac: float = 0.10
+    summary_noise: float = 0.1
+    anchor_perturb: float = 0.1
+    build_slot: int = -1            # slot filled by the state builder (-1: none)
+    visual: Optional[Tuple[int, int, int, float]] = None   # (start, stop, clusters, sigma)
+    seed: int = 20260929
+
+    @property
+    def S(self) -> int:
+        return len(self.seg_len)
+
+    @property
+    def edges(self) -> int:
+        return self.n_agents - 1
+
+    @property
+    def max_seg_len(self) -> int:
+        return max(self.seg_len) if self.seg_len else 0
+
+    @property
+    def k_top(self) -> int:
+        return self.top_k if self.top_k > 0 else self.A
+
+    @property
+    def l(self) -> int:
+        return self.r + self.oversample
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    @property
+    def ph_tokens(self) -> int:
+        return int(sum(self.seg_len))
+
+
+def _uniform_segments(R: int, n_per_req: int, pf: int, ph: int):
+    req, start, length = [], [], []
+    for q in range(R):
+        for i in range(n_per_req):
+            req.append(q)
+            start.append(i * (pf + ph) + pf)
+            length.append(ph)
+    return tuple(req), tuple(start), tuple(length)
+
+
+def _build_workloads() -> Dict[str, Workload]:
+    w = {}
+    w["tiny"] = Workload(
+        name="tiny", L=1, H=2, d=64, dtype="f32", R=1, T=256,
+        seg_request=(0,), seg_start=(0,), seg_len=(256,), n_agents=2,
+        A=2, r=8, tau=0.3, delta="planted",
+        planted_s=(2.0, 1.0, 0.5, 0.25), noise=0.01, fallback_frac=0.0,
+        build_slot=0, seed=20260929 + 0)
+    req, st, ln = _uniform_segments(10, 1, 0, 2048)
+    w["llama2k"] = Workload(
+        name="llama2k", L=32, H=8, d=128, dtype="bf16", R=10, T=2048,
+        seg_request=req, seg_start=st, seg_len=ln, n_agents=4,
+        A=8, r=32, tau=0.32, fallback_frac=0.10, seed=20260929 + 1)
+    req, st, ln = _uniform_segments(16, 16, 128, 512)
+    w["concurrent"] = Workload(
+        name="concurrent", L=32, H=8, d=128, dtype="bf16", R=16, T=16 * 640,
+        seg_request=req, seg_start=st, seg_len=ln, n_agents=4,
+        A=8, r=32, tau=0.32, fallback_frac=0.10, seed=20260929 + 2)
+    req, st, ln = _uniform_segments(1, 64, 0, 512)
+    w["longctx"] = Workload(
+        name="longctx", L=32, H=8, d=128, dtype="bf16", R=1, T=32768,
+        seg_request=req, seg_start=st, seg_len=ln, n_agents=4,
+        A=16, r=32, tau=0.32, fallback_frac=0.10, build_slot=0,
+        seed=20260929 + 3)
+    st = tuple(512 * i for i in range(18))
+    ln = tuple([512] * 17 + [296])
+    w["vl"] = Workload(
+        name="vl", L=28, H=4, d=128, dtype="bf16", R=1, T=9000,
+        seg_request=tuple([0] * 18), seg_start=st, seg_len=ln, n_agents=4,
+        A=8, r=32, tau=0.6, fallback_frac=0.20,
+        visual=(1024, 7024, 64, 0.3), seed=20260929 + 4)
+    return w
+
+
+WORKLOADS: Dict[str, Workload] = _build_workloads()
+
+
+def workload(name: str) -> Workload:
+    return WORKLOADS[name]
+
+
+def scaled(base: Workload, *, L: Optional[int] = None, H: Optional[int] = None,
+           R: Optional[int] = None, seg_len: Optional[Sequence[int]] = None,
+           pf: int = 0, segs_per_req: int = 1, **overrides) -> Workload:
+    """A smaller workload with the same structure (for oracle-sized parity).
+
+    ``seg_len`` lists the PH segment lengths of one request; each is preceded
+    by a ``pf``-token agent-specific prefix segment.  ``segs_per_req`` repeats
+    the list.  Any other field may be overridden by keyword.
+    """
+    L = base.L if L is None else L
+    H = base.H if H is None else H
+    R = base.R if R is None else R
+    lens = list(seg_len) if seg_len is not None else [base.seg_len[0]]
+    lens = lens * segs_per_req
+    req, start, length = [], [], []
+    T = 0
+    for q in range(R):
+        pos = 0
+        for sl in lens:
+            pos += pf
+            req.append(q)
+            start.append(pos)
+            length.append(sl)
+            pos += sl
+        T = max(T, pos)
+    fields = dict(L=L, H=H, R=R, T=T, seg_request=tuple(req),
+                  seg_start=tuple(start), seg_len=tuple(length),
+                  name=overrides.pop("name", base.name + "-scaled"))
+    vis = base.visual
+    if vis is not None:
+        lo, hi = int(0.11 * T), int(0.78 * T)     # same proportions as 1024..7024 of 9000
+        vis = (lo, max(hi, lo + 1), vis[2], vis[3])
+        fields["visual"] = vis
+    fields.update(overrides)
+    return dataclasses.replace(base, **fields)
+
+
+def segment_arrays(wl: Workload):
+    """int32 numpy arrays (seg_request, seg_start, seg_len)."""
+    return (np.asarray(wl.seg_request, dtype=np.int32),
+            np.asarray(wl.seg_start, dtype=np.int32),
+            np.asarray(wl.seg_len, dtype=np.int32))
+
+
+# --------------------------------------------------------------------------
+# seeded generators
+# --------------------------------------------------------------------------
+_PURPOSE = {"base": 1, "pf": 2, "delta": 3, "anchor": 4, "summary": 5,
+            "omega": 6, "planted": 7, "visual": 8}
+
+
+def _generator(device: torch.device, wl: Workload, purpose: str, *key: int) -> torch.Generator:
+    ss = np.random.SeedSequence([wl.seed, _PURPOSE[purpose], *[int(k) for k in key]])
+    g = torch.Generator(device=device)
+    g.manual_seed(int(ss.generate_state(1, dtype=np.uint64)[0] & 0x7FFFFFFFFFFFFFFF))
+    return g
+
+
+def _randn(shape, g: torch.Generator, device) -> torch.Tensor:
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+
+
+def _haar(batch: int, n: int, m: int, g: torch.Generator, device) -> torch.Tensor:
+    """Haar-distributed n x m matrices with orthonormal columns (m <= n).
+
+    QR of a Gaussian matrix with the column signs fixed by sign(diag R)
+    (Mezzadri, "How to generate random matrices from the classical compact
+    groups", Notices AMS 2007)."""
+    G = _randn((batch, n, m), g, device)
+    Q, Rm = torch.linalg.qr(G, mode="reduced")
+    sgn = torch.sign(torch.diagonal(Rm, dim1=-2, dim2=-1))
+    sgn = torch.where(sgn == 0, torch.ones_like(sgn), sgn)
+    return Q * sgn.unsqueeze(-2)
+
+
+# --------------------------------------------------------------------------
+# generated tensors
+# --------------------------------------------------------------------------
+@dataclass
+class EdgeInputs:
+    """Inputs of workflow edge j -> j+1 (edge index j+1 in 1..E).
+
+    U_*: [S, L, H, Tmax, A, r]  token factors (singular values folded in)
+    W_*: [S, L, H, d, A, r]     feature factors
+    summaries: [S, L, H, A, d] float32 anchor summaries
+    planted: [S] bool, segments whose delta was scaled to exceed tau
+    """
+    U_K: torch.Tensor
+    W_K: torch.Tensor
+    U_V: torch.Tensor
+    W_V: torch.Tensor
+    summaries: torch.Tensor
+    planted: torch.Tensor
+
+
+@dataclass
+class WorkloadInputs:
+    wl: Workload
+    exact_K: List[torch.Tensor]      # agent caches E_0 .. E_{n-1}, [R, L, H, T, d]
+    exact_V: List[torch.Tensor]
+    edges: List[EdgeInputs]          # edge j (1-based) at index j-1
+    omega: torch.Tensor              # [d, l] float32 test matrix for the builder
+    planted_ratio: Tuple[float, float]
+
+
+def _seg_ratio(wl: Workload, planted: bool) -> float:
+    """Target ratio |Delta_r|_F / |ref|_F for a unit of a segment.
+
+    Reused segments sit at 0.4 tau and planted ones at 1.9 tau, so that the
+    segment-level reliability score stays far (>= 25%) from tau even after the
+    +-10% anchor perturbation."""
+    return wl.tau * (1.9 if planted else 0.4)
+
+
+def generate(wl: Workload, device="cpu", edges: Optional[Sequence[int]] = None) -> WorkloadInputs:
+    """Generate every agent's exact cache and every edge's anchor inputs.
+
+    ``edges`` restricts which edges get anchor inputs (others are None); the
+    exact caches of all agents are always generated (they chain)."""
+    device = torch.device(device)
+    dt = wl.torch_dtype
+    R, L, H, T, d = wl.R, wl.L, wl.H, wl.T, wl.d
+    S, A, r = wl.S, wl.A, wl.r
+    Tm = wl.max_seg_len
+    E = wl.edges
+    want = set(range(1, E + 1)) if edges is None else set(int(e) for e in edges)
+
+    # ---- base cache E_0 (agent A0 prefills exactly) ----
+    K0 = torch.empty((R, L, H, T, d), dtype=dt, device=device)
+    V0 = torch.empty((R, L, H, T, d), dtype=dt, device=device)
+    for q in range(R):
+        g = _generator(device, wl, "base", q)
+        kq = _randn((L, H, T, d), g, device)
+        vq = _randn((L, H, T, d), g, device)
+        if wl.visual is not None:
+            lo, hi, ncl, sig = wl.visual
+            gv = _generator(device, wl, "visual", q)
+            centres = _randn((L, H, ncl, d), gv, device)
+            assign = torch.randint(0, ncl, (L, H, hi - lo), generator=gv, device=device)
+            idx = assign.unsqueeze(-1).expand(L, H, hi - lo, d)
+            kq[:, :, lo:hi, :] = torch.gather(centres, 2, idx) + sig * _randn((L, H, hi - lo, d), gv, device)
+        K0[q] = kq.to(dt)
+        V0[q] = vq.to(dt)
+        del kq, vq
+
+    # planted (fallback) segments per edge: a seeded choice of round(frac * S)
+    planted_masks = []
+    for j in range(1, E + 1):
+        n_pl = int(round(wl.fallback_frac * S))
+        g = _generator(torch.device("cpu"), wl, "planted", j)
+        perm = torch.randperm(S, generator=g)
+        m = torch.zeros(S, dtype=torch.bool)
+        m[perm[:n_pl]] = True
+        planted_masks.append(m)
+
+    exact_K = [K0]
+    exact_V = [V0]
+    edge_inputs: List[Optional[EdgeInputs]] = []
+    ph_mask = torch.zeros((R, T), dtype=torch.bool)
+    for s in range(S):
+        ph_mask[wl.seg_request[s], wl.seg_start[s]:wl.seg_start[s] + wl.seg_len[s]] = True
+    pf_exists = bool((~ph_mask).any())
+
+    for j in range(1, E + 1):
+        prevK, prevV = exact_K[-1], exact_V[-1]
+        Kj = prevK.clone()
+        Vj = prevV.clone()
+        if pf_exists:
+            # agent-specific prefix rows: each agent prefills its own PF segments
+            for q in range(R):
+                g = _generator(device, wl, "pf", j, q)
+                pfm = (~ph_mask[q]).to(device)
+                npf = int(pfm.sum())
+                if npf:
+                    Kj[q][:, :, pfm, :] = _randn((L, H, npf, d), g, device).to(dt)
+                    Vj[q][:, :, pfm, :] = _randn((L, H, npf, d), g, device).to(dt)
+        ein = None
+        if j in want:
+            U_K = torch.zeros((S, L, H, Tm, A, r), dtype=dt, device=device)
+            U_V = torch.zeros_like(U_K)
+            W_K = torch.zeros((S, L, H, d, A, r), dtype=dt, device=device)
+            W_V = torch.zeros_like(W_K)
+            summ = torch.zeros((S, L, H, A, d), dtype=torch.float32, device=device)
+        for s in range(S):
+            q, t0, n = wl.seg_request[s], wl.seg_start[s], wl.seg_len[s]
+            planted = bool(planted_masks[j - 1][s])
+            g = _generator(device, wl, "delta", j, s)
+            for kv, (prev, cur) in enumerate(((prevK, Kj), (prevV, Vj))):
+                ref_rows = prev[q, :, :, t0:t0 + n, :].float()          # [L, H, n, d]
+                m = min(n, d)
+                if wl.delta == "planted":
+                    sv = torch.tensor(wl.planted_s, dtype=torch.float32, device=device)
+                    m = min(m, sv.numel())
+                    sv = sv[:m].expand(L, H, m)
+                else:
+                    geo = wl.decay ** torch.arange(m, dtype=torch.float32, device=device)
+                    rr = min(r, m)
+                    ratio = _seg_ratio(wl, planted)
+                    refn = torch.linalg.vector_norm(ref_rows, dim=(-2, -1))   # [L, H]
+                    c = ratio * refn / torch.sqrt((geo[:rr] ** 2).sum())
+                    sv = c.unsqueeze(-1) * geo                                # [L, H, m]
+                Uh = _haar(L * H, n, m, g, device).reshape(L, H, n, m)
+                Vh = _haar(L * H, d, m, g, device).reshape(L, H, d, m)
+                delta = torch.matmul(Uh * sv.unsqueeze(-2), Vh.transpose(-1, -2))
+                delta = delta + wl.noise * _randn((L, H, n, d), g, device)
+                cur[q, :, :, t0:t0 + n, :] = (ref_rows + delta).to(dt)
+                if j in want:
+                    ga = _generator(device, wl, "anchor", j, s, kv)
+                    rr = min(r, m)
+                    Ut = Uh[..., :rr] * sv[..., :rr].unsqueeze(-2)          # [L, H, n, rr]
+                    Wt = Vh[..., :rr]                                         # [L, H, d, rr]
+                    un = torch.linalg.vector_norm(Ut, dim=(-2, -1), keepdim=True)
+                    wn = math.sqrt(rr)
+                    eps = wl.anchor_perturb / math.sqrt(2.0)
+                    Uo = U_K if kv == 0 else U_V
+                    Wo = W_K if kv == 0 else W_V
+                    for a in range(A):
+                        pu = _randn((L, H, n, rr), ga, device)
+                        pw = _randn((L, H, d, rr), ga, device)
+                        pu = pu * (eps * un / torch.linalg.vector_norm(pu, dim=(-2, -1), keepdim=True))
+                        pw = pw * (eps * wn / torch.linalg.vector_norm(pw, dim=(-2, -1), keepdim=True))
+                        Uo[s, :, :, :n, a, :rr] = (Ut + pu).to(dt)
+                        Wo[s, :, :, :, a, :rr] = (Wt + pw).to(dt)
+                del delta, Uh, Vh, ref_rows
+            if j in want:
+                gs = _generator(device, wl, "summary", j, s)
+                kmean = prevK[q, :, :, t0:t0 + n, :].float().mean(dim=2)      # [L, H, d]
+                summ[s] = kmean.unsqueeze(2) + wl.summary_noise * _randn((L, H, A, d), gs, device)
+        if j in want:
+            ein = EdgeInputs(U_K=U_K, W_K=W_K, U_V=U_V, W_V=W_V, summaries=summ,
+                             planted=planted_masks[j - 1].clone())
+        edge_inputs.append(ein)
+        exact_K.append(Kj)
+        exact_V.append(Vj)
+
+    go = _generator(device, wl, "omega")
+    omega = _randn((d, wl.l), go, device)
+    return WorkloadInputs(wl=wl, exact_K=exact_K, exact_V=exact_V, edges=edge_inputs,
+                          omega=omega, planted_ratio=(_seg_ratio(wl, False), _seg_ratio(wl, True)))
