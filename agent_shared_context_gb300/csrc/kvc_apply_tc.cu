@@ -1,0 +1,598 @@
+// kvc_apply_tc.cu -- K3 for bf16 caches: the fused correction apply on
+// tcgen05 tensor cores (KVCMAS listing, Figure 1(a)-(b)).
+//
+// Work item = one (segment, layer, KV head, K|V) block; a persistent grid of
+// one CTA per SM walks the items.  For an item with n tokens the correction
+// is the skinny product C[n, d] = U[n, A*r] . (w (.) W)[A*r, d]^T, where the
+// anchor weights are folded into W once per item.  Per 128-token tile:
+//
+//   warp 0 (1 thread)  TMA: the item's W chunks (once), the ref tile and the
+//                      U chunks (64 columns = one 128-byte swizzle row each)
+//                      into shared-memory rings guarded by mbarriers;
+//   warp 1 (1 thread)  tcgen05.mma kind::f16, M = 128 tokens, N = d,
+//                      K = A*r in steps of 16, accumulating in TMEM (two
+//                      accumulator buffers so tile t+1's MMAs overlap tile
+//                      t's epilogue);
+//   warps 2-5          fold the weights into W in place (bf16, RNE) once per
+//                      item; per tile read the fp32 accumulator rows from
+//                      TMEM (thread = token row), add the ref row from shared
+//                      memory, round to bf16 (RNE), accumulate |C|^2 and
+//                      |ref|^2, write the result over the ref tile and TMA-
+//                      store it (full tiles) or store the valid rows with
+//                      16-byte stores (the ragged tail tile).
+//
+// Per-item norms are reduced in a fixed order and written to partial[unit,
+// kv] / partial[unit, 2 + kv]; K4 turns them into the segment score.
+//
+// Every wait is bounded (kWaitLimitNs); a wait that expires stores
+// KVC_ERR_DEVICE_TIMEOUT into *dev_status, raises a CTA-wide abort flag so
+// the other roles stop, drains the copies and MMAs already issued, frees TMEM
+// and returns.
+#include <cuda_bf16.h>
+
+#include <cstring>
+
+#include "kvc_internal.h"
+#include "kvc_ptx.cuh"
+
+namespace kvc {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;                   // tokens per tile (MMA M)
+constexpr int kChunk = 64;                 // bf16 per 128-byte swizzled row
+constexpr int kUStageBytes = kBM * 128;    // one U chunk: 128 rows x 128 B
+constexpr int kThreads = 192;
+constexpr int kMaxUStages = 8;
+constexpr int kMaxRefBufs = 2;
+constexpr int kEpiThreads = 128;
+
+struct TcMaps {
+  CUtensorMap ref[2];
+  CUtensorMap out[2];
+  CUtensorMap U[2];
+  CUtensorMap W[2];
+};
+
+struct TcArgs {
+  char* out[2];              // bases for the masked tail stores
+  int64_t os[2][4];          // out element strides (req, layer, head, tok)
+  const float* weights;      // [units, A]
+  float* partial;            // [units, 4]
+  int32_t* dev_status;
+  int32_t L, H, A, r, K, KC, n_items, n_ustages, n_refbufs;
+};
+
+struct Bars {
+  uint64_t w_full, w_ready, w_free, mma_drain;
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t u_full[kMaxUStages], u_empty[kMaxUStages];
+  uint64_t ref_full[kMaxRefBufs], ref_empty[kMaxRefBufs];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int32_t epi_ok;
+  float red[2][4];
+};
+
+struct Item {
+  int unit, kv, s, l, h, req, start, len, ntiles;
+};
+
+__device__ __forceinline__ Item decode_item(int it, const TcArgs& a, const SegTable& seg) {
+  Item x;
+  x.kv = it & 1;
+  x.unit = it >> 1;
+  x.h = x.unit % a.H;
+  x.l = (x.unit / a.H) % a.L;
+  x.s = x.unit / (a.H * a.L);
+  x.req = seg.req[x.s];
+  x.start = seg.start[x.s];
+  x.len = seg.len[x.s];
+  x.ntiles = (x.len + kBM - 1) / kBM;
+  return x;
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Bounded wait; on expiry records the timeout once and raises the abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* bars,
+                                              int32_t* dev_status) {
+  if (mbar_wait_bounded(bar, parity, kWaitLimitNs, &bars->abort_flag)) return true;
+  volatile int32_t* ab = &bars->abort_flag;
+  if (*ab == 0) {
+    *ab = 1;
+    atomicCAS(dev_status, 0, static_cast<int32_t>(KVC_ERR_DEVICE_TIMEOUT));
+  }
+  return false;
+}
+
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float w) {
+  __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(p[i]);
+    f.x *= w;
+    f.y *= w;
+    p[i] = __float22bfloat162_rn(f);
+  }
+  return v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    apply_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a,
+                    const __grid_constant__ SegTable seg) {
+  constexpr int WCB = D * 128;               // one W chunk: D rows x 128 B
+  constexpr int REFB = kBM * D * 2;          // one ref/out tile
+  constexpr int NSUB = D / kChunk;           // 64-column sub-boxes per tile
+  constexpr uint32_t kTmemCols = 2 * D;      // two fp32 accumulators of D columns
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, D);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* w_smem = smem;
+  uint8_t* u_smem = w_smem + a.KC * WCB;
+  uint8_t* r_smem = u_smem + a.n_ustages * kUStageBytes;
+  Bars* bars = reinterpret_cast<Bars*>(r_smem + a.n_refbufs * REFB);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int NSU = a.n_ustages;
+  const int NRB = a.n_refbufs;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->w_full, 1);
+    mbar_init(&bars->w_ready, 1);
+    mbar_init(&bars->w_free, 1);
+    mbar_init(&bars->mma_drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->acc_full[b], 1);
+      mbar_init(&bars->acc_empty[b], 1);
+    }
+    for (int i = 0; i < NSU; ++i) {
+      mbar_init(&bars->u_full[i], 1);
+      mbar_init(&bars->u_empty[i], 1);
+    }
+    for (int i = 0; i < NRB; ++i) {
+      mbar_init(&bars->ref_full[i], 1);
+      mbar_init(&bars->ref_empty[i], 1);
+    }
+    bars->abort_flag = 0;
+    bars->epi_ok = 1;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int kv = 0; kv < 2; ++kv) {
+        tma_prefetch_desc(&maps.ref[kv]);
+        tma_prefetch_desc(&maps.U[kv]);
+        tma_prefetch_desc(&maps.W[kv]);
+        tma_prefetch_desc(&maps.out[kv]);
+      }
+      uint32_t ust = 0, uph = 0, rb = 0, rph = 0, wfree_ph = 0;
+      uint32_t u_last[kMaxUStages], r_last[kMaxRefBufs];
+      bool u_used[kMaxUStages], r_used[kMaxRefBufs];
+      for (int i = 0; i < kMaxUStages; ++i) u_used[i] = false;
+      for (int i = 0; i < kMaxRefBufs; ++i) r_used[i] = false;
+      bool w_used = false;
+      uint32_t w_last = 0, w_issue_count = 0;
+      bool ok = true;
+      const int w_after = a.KC < NSU ? a.KC : NSU;
+      for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x) {
+        const Item x = decode_item(it, a, seg);
+        bool w_issued = false;
+        int uc = 0;
+        auto issue_w = [&]() {
+          if (w_issue_count > 0) {
+            if (!wait_or_abort(&bars->w_free, wfree_ph, bars, a.dev_status)) {
+              ok = false;
+              return;
+            }
+            wfree_ph ^= 1u;
+          }
+          mbar_arrive_expect_tx(&bars->w_full, static_cast<uint32_t>(a.KC * WCB));
+          for (int kc = 0; kc < a.KC; ++kc)
+            tma_load_3d(w_smem + kc * WCB, &maps.W[x.kv], &bars->w_full, kc * kChunk, 0, x.unit);
+          w_last = w_issue_count & 1u;
+          w_used = true;
+          ++w_issue_count;
+          w_issued = true;
+        };
+        for (int t = 0; t < x.ntiles && ok; ++t) {
+          if (!wait_or_abort(&bars->ref_empty[rb], rph ^ 1u, bars, a.dev_status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->ref_full[rb], static_cast<uint32_t>(REFB));
+#pragma unroll
+          for (int sub = 0; sub < NSUB; ++sub)
+            tma_load_5d(r_smem + rb * REFB + sub * (kBM * 128), &maps.ref[x.kv],
+                        &bars->ref_full[rb], sub * kChunk, x.start + t * kBM, x.h, x.l, x.req);
+          r_last[rb] = rph;
+          r_used[rb] = true;
+          if (++rb == static_cast<uint32_t>(NRB)) {
+            rb = 0;
+            rph ^= 1u;
+          }
+          for (int kc = 0; kc < a.KC; ++kc) {
+            if (!w_issued && uc == w_after) {
+              issue_w();
+              if (!ok) break;
+            }
+            if (!wait_or_abort(&bars->u_empty[ust], uph ^ 1u, bars, a.dev_status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bars->u_full[ust], static_cast<uint32_t>(kUStageBytes));
+            tma_load_3d(u_smem + ust * kUStageBytes, &maps.U[x.kv], &bars->u_full[ust],
+                        kc * kChunk, t * kBM, x.unit);
+            u_last[ust] = uph;
+            u_used[ust] = true;
+            if (++ust == static_cast<uint32_t>(NSU)) {
+              ust = 0;
+              uph ^= 1u;
+            }
+            ++uc;
+          }
+        }
+        if (ok && !w_issued) issue_w();
+      }
+      // Drain: every copy issued into this CTA's shared memory must land
+      // before the CTA may exit (bounded; a no-op after normal completion).
+      for (int i = 0; i < NSU; ++i)
+        if (u_used[i]) (void)mbar_wait_bounded(&bars->u_full[i], u_last[i], kWaitLimitNs);
+      for (int i = 0; i < NRB; ++i)
+        if (r_used[i]) (void)mbar_wait_bounded(&bars->ref_full[i], r_last[i], kWaitLimitNs);
+      if (w_used) (void)mbar_wait_bounded(&bars->w_full, w_last, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t ust = 0, uph = 0, wr_ph = 0, tile_count = 0;
+      uint32_t acc_eph[2] = {0u, 0u};
+      bool ok = true;
+      bool issued_any = false;
+      for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x) {
+        const Item x = decode_item(it, a, seg);
+        if (!wait_or_abort(&bars->w_ready, wr_ph, bars, a.dev_status)) {
+          ok = false;
+          break;
+        }
+        wr_ph ^= 1u;
+        tc_fence_after();
+        for (int t = 0; t < x.ntiles && ok; ++t) {
+          const uint32_t b = tile_count & 1u;
+          if (!wait_or_abort(&bars->acc_empty[b], acc_eph[b] ^ 1u, bars, a.dev_status)) {
+            ok = false;
+            break;
+          }
+          acc_eph[b] ^= 1u;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + b * static_cast<uint32_t>(D);
+          for (int kc = 0; kc < a.KC; ++kc) {
+            if (!wait_or_abort(&bars->u_full[ust], uph, bars, a.dev_status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(u_smem + ust * kUStageBytes);
+            const uint32_t b_base = smem_u32(w_smem + kc * WCB);
+            const int rem = a.K - kc * kChunk;
+            const int nks = rem >= kChunk ? 4 : (rem + 15) / 16;
+            for (int ks = 0; ks < nks; ++ks) {
+              mma_bf16_ss(d_tmem, desc_kmajor_sw128(a_base + ks * 32),
+                          desc_kmajor_sw128(b_base + ks * 32), kIdesc,
+                          (kc | ks) != 0 ? 1u : 0u);
+            }
+            issued_any = true;
+            mma_commit(&bars->u_empty[ust]);
+            if (++ust == static_cast<uint32_t>(NSU)) {
+              ust = 0;
+              uph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit(&bars->acc_full[b]);
+          ++tile_count;
+        }
+        if (!ok) break;
+        mma_commit(&bars->w_free);
+      }
+      // Drain: all MMAs issued by this thread complete before TMEM is freed.
+      if (issued_any) {
+        mma_commit(&bars->mma_drain);
+        (void)mbar_wait_bounded(&bars->mma_drain, 0, kWaitLimitNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 64;          // 0..127
+    const int q = warp & 3;                   // TMEM lane quadrant of this warp
+    const int m = q * 32 + lane;              // token row of the tile
+    uint32_t wf_ph = 0, rph = 0, rb = 0, tile_count = 0;
+    uint32_t acc_fph[2] = {0u, 0u};
+    volatile int32_t* epi_ok = &bars->epi_ok;
+    // One thread waits (bounded) and broadcasts the outcome; the others then
+    // re-check the completed phase, which returns at once and orders their
+    // reads after the producer's writes.
+    auto epi_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (et == 0) *epi_ok = wait_or_abort(bar, parity, bars, a.dev_status) ? 1 : 0;
+      named_sync(1, kEpiThreads);
+      const bool ok = *epi_ok != 0;
+      if (ok && et != 0) (void)mbar_wait_bounded(bar, parity, kWaitLimitNs);
+      named_sync(1, kEpiThreads);
+      return ok;
+    };
+    for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
+      const Item x = decode_item(it, a, seg);
+      if (!epi_wait(&bars->w_full, wf_ph)) break;
+      wf_ph ^= 1u;
+      // Fold the anchor weights into W (in place, bf16 RNE).  W chunk kc
+      // holds D rows of 64 K-values; 16-byte unit p of row n holds K-group
+      // p ^ (n & 7) (128-byte swizzle).
+      {
+        const float* wts = a.weights + static_cast<int64_t>(x.unit) * a.A;
+        const int per_chunk = WCB / 16;
+        const int total = a.KC * per_chunk;
+        for (int idx = et; idx < total; idx += kEpiThreads) {
+          const int kc = idx / per_chunk;
+          const int rem = idx - kc * per_chunk;
+          const int nrow = rem >> 3;
+          const int j = (rem & 7) ^ (nrow & 7);
+          const int k = kc * kChunk + j * 8;
+          if (k < a.K) {
+            uint4* p = reinterpret_cast<uint4*>(w_smem + static_cast<size_t>(idx) * 16);
+            *p = scale_bf16x8(*p, __ldg(wts + k / a.r));
+          }
+        }
+        fence_proxy_async_smem();
+        named_sync(1, kEpiThreads);
+        if (et == 0) mbar_arrive(&bars->w_ready);
+      }
+      float c2 = 0.0f, r2 = 0.0f;
+      bool ok = true;
+      for (int t = 0; t < x.ntiles; ++t) {
+        const uint32_t b = tile_count & 1u;
+        if (!epi_wait(&bars->acc_full[b], acc_fph[b])) {
+          ok = false;
+          break;
+        }
+        acc_fph[b] ^= 1u;
+        tc_fence_after();
+        if (!epi_wait(&bars->ref_full[rb], rph)) {
+          ok = false;
+          break;
+        }
+        const int rows_valid = min(kBM, x.len - t * kBM);
+        uint8_t* rt = r_smem + rb * REFB;
+        const bool row_ok = m < rows_valid;
+#pragma unroll 1
+        for (int cb = 0; cb < D / 16; ++cb) {
+          uint32_t v[16];
+          __syncwarp();
+          tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(q * 32) << 16) + b * D + cb * 16, v);
+          tmem_ld_wait();
+          const int col0 = cb * 16;
+          const int sub = col0 / kChunk;
+          const int j0 = (col0 % kChunk) / 8;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int j = j0 + u;
+            uint4* p = reinterpret_cast<uint4*>(rt + sub * (kBM * 128) + m * 128 +
+                                                ((j ^ (m & 7)) << 4));
+            uint4 rv = *p;
+            __nv_bfloat162* rp = reinterpret_cast<__nv_bfloat162*>(&rv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 rf = __bfloat1622float2(rp[e]);
+              const float cx = __uint_as_float(v[u * 8 + 2 * e]);
+              const float cy = __uint_as_float(v[u * 8 + 2 * e + 1]);
+              if (row_ok) {
+                c2 = fmaf(cx, cx, c2);
+                c2 = fmaf(cy, cy, c2);
+                r2 = fmaf(rf.x, rf.x, r2);
+                r2 = fmaf(rf.y, rf.y, r2);
+              }
+              rp[e] = __float22bfloat162_rn(make_float2(rf.x + cx, rf.y + cy));
+            }
+            *p = rv;
+          }
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        named_sync(1, kEpiThreads);
+        if (et == 0) mbar_arrive(&bars->acc_empty[b]);
+        if (rows_valid == kBM) {
+          if (et == 0) {
+#pragma unroll
+            for (int sub = 0; sub < NSUB; ++sub)
+              tma_store_5d(&maps.out[x.kv], rt + sub * (kBM * 128), sub * kChunk,
+                           x.start + t * kBM, x.h, x.l, x.req);
+            bulk_commit_group();
+            bulk_wait_group_read<0>();
+            mbar_arrive(&bars->ref_empty[rb]);
+          }
+        } else {
+          if (row_ok) {
+            const int64_t e2 = 2;
+            char* orow = a.out[x.kv] +
+                         (static_cast<int64_t>(x.req) * a.os[x.kv][0] +
+                          static_cast<int64_t>(x.l) * a.os[x.kv][1] +
+                          static_cast<int64_t>(x.h) * a.os[x.kv][2] +
+                          static_cast<int64_t>(x.start + t * kBM + m) * a.os[x.kv][3]) *
+                             e2;
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j) {
+              const int sub = j / 8, jj = j % 8;
+              const uint4 val = *reinterpret_cast<const uint4*>(
+                  rt + sub * (kBM * 128) + m * 128 + ((jj ^ (m & 7)) << 4));
+              reinterpret_cast<uint4*>(orow)[j] = val;
+            }
+          }
+          named_sync(1, kEpiThreads);
+          if (et == 0) mbar_arrive(&bars->ref_empty[rb]);
+        }
+        if (++rb == static_cast<uint32_t>(NRB)) {
+          rb = 0;
+          rph ^= 1u;
+        }
+        ++tile_count;
+      }
+      if (!ok) break;
+      // fixed-order reduction of the item's norms
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        c2 += __shfl_xor_sync(0xffffffffu, c2, o);
+        r2 += __shfl_xor_sync(0xffffffffu, r2, o);
+      }
+      if (lane == 0) {
+        bars->red[0][q] = c2;
+        bars->red[1][q] = r2;
+      }
+      named_sync(1, kEpiThreads);
+      if (et == 0) {
+        const float sc = ((bars->red[0][0] + bars->red[0][1]) + bars->red[0][2]) + bars->red[0][3];
+        const float sr = ((bars->red[1][0] + bars->red[1][1]) + bars->red[1][2]) + bars->red[1][3];
+        a.partial[static_cast<int64_t>(x.unit) * 4 + x.kv] = sc;
+        a.partial[static_cast<int64_t>(x.unit) * 4 + 2 + x.kv] = sr;
+      }
+      named_sync(1, kEpiThreads);
+    }
+    if (et == 0) bulk_wait_group<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int D>
+cudaError_t launch_d(const Dims& dm, const SegTable& seg, const View refv[2], const View outv[2],
+                     const void* U[2], const void* W[2], const float* weights, float* partial,
+                     int32_t* dev_status, cudaStream_t stream) {
+  DeviceInfo di{};
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  const int K = dm.A * dm.r;
+  const int KC = (K + kChunk - 1) / kChunk;
+  constexpr int WCB = D * 128;
+  constexpr int REFB = kBM * D * 2;
+  const size_t fixed = 1024 + sizeof(Bars) + 64;
+  const size_t budget = static_cast<size_t>(di.max_smem_optin);
+  int nrb = 2, nsu = 0;
+  for (; nrb >= 1; --nrb) {
+    const size_t used = fixed + static_cast<size_t>(KC) * WCB + static_cast<size_t>(nrb) * REFB;
+    if (used >= budget) continue;
+    nsu = static_cast<int>((budget - used) / kUStageBytes);
+    if (nsu > kMaxUStages) nsu = kMaxUStages;
+    if (nsu >= 3 || (nrb == 1 && nsu >= 2)) break;
+  }
+  if (nrb < 1 || nsu < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = fixed + static_cast<size_t>(KC) * WCB + static_cast<size_t>(nrb) * REFB +
+                      static_cast<size_t>(nsu) * kUStageBytes;
+
+  TcMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  const uint64_t units = static_cast<uint64_t>(dm.units());
+  for (int kv = 0; kv < 2; ++kv) {
+    {
+      const uint64_t dims[5] = {static_cast<uint64_t>(dm.d), static_cast<uint64_t>(dm.T),
+                                static_cast<uint64_t>(dm.H), static_cast<uint64_t>(dm.L),
+                                static_cast<uint64_t>(dm.R)};
+      const uint32_t box[5] = {kChunk, kBM, 1, 1, 1};
+      const uint64_t rs[4] = {static_cast<uint64_t>(refv[kv].s_tok) * 2,
+                              static_cast<uint64_t>(refv[kv].s_head) * 2,
+                              static_cast<uint64_t>(refv[kv].s_layer) * 2,
+                              static_cast<uint64_t>(refv[kv].s_req) * 2};
+      e = encode_tiled(&maps.ref[kv], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, refv[kv].base, dims, rs,
+                       box, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (e != cudaSuccess) return e;
+      const uint64_t os[4] = {static_cast<uint64_t>(outv[kv].s_tok) * 2,
+                              static_cast<uint64_t>(outv[kv].s_head) * 2,
+                              static_cast<uint64_t>(outv[kv].s_layer) * 2,
+                              static_cast<uint64_t>(outv[kv].s_req) * 2};
+      e = encode_tiled(&maps.out[kv], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, outv[kv].base, dims, os,
+                       box, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (e != cudaSuccess) return e;
+    }
+    {
+      const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(dm.Tmax), units};
+      const uint64_t st[2] = {static_cast<uint64_t>(K) * 2,
+                              static_cast<uint64_t>(dm.Tmax) * static_cast<uint64_t>(K) * 2};
+      const uint32_t box[3] = {kChunk, kBM, 1};
+      e = encode_tiled(&maps.U[kv], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(U[kv]),
+                       dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (e != cudaSuccess) return e;
+    }
+    {
+      const uint64_t dims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(D), units};
+      const uint64_t st[2] = {static_cast<uint64_t>(K) * 2,
+                              static_cast<uint64_t>(D) * static_cast<uint64_t>(K) * 2};
+      const uint32_t box[3] = {kChunk, static_cast<uint32_t>(D), 1};
+      e = encode_tiled(&maps.W[kv], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(W[kv]),
+                       dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (e != cudaSuccess) return e;
+    }
+  }
+
+  TcArgs a{};
+  for (int kv = 0; kv < 2; ++kv) {
+    a.out[kv] = static_cast<char*>(outv[kv].base);
+    a.os[kv][0] = outv[kv].s_req;
+    a.os[kv][1] = outv[kv].s_layer;
+    a.os[kv][2] = outv[kv].s_head;
+    a.os[kv][3] = outv[kv].s_tok;
+  }
+  a.weights = weights;
+  a.partial = partial;
+  a.dev_status = dev_status;
+  a.L = dm.L;
+  a.H = dm.H;
+  a.A = dm.A;
+  a.r = dm.r;
+  a.K = K;
+  a.KC = KC;
+  const int64_t items = dm.units() * 2;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  a.n_items = static_cast<int32_t>(items);
+  a.n_ustages = nsu;
+  a.n_refbufs = nrb;
+
+  e = cudaFuncSetAttribute(apply_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(items < di.sm_count ? items : di.sm_count);
+  apply_tc_kernel<D><<<grid, kThreads, smem, stream>>>(maps, a, seg);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_apply_tc(const Dims& dm, const SegTable& seg, const View refv[2],
+                            const View outv[2], const void* U[2], const void* W[2],
+                            const float* weights, float* partial, int32_t* dev_status,
+                            cudaStream_t stream) {
+  if (dm.d == 128)
+    return launch_d<128>(dm, seg, refv, outv, U, W, weights, partial, dev_status, stream);
+  if (dm.d == 64)
+    return launch_d<64>(dm, seg, refv, outv, U, W, weights, partial, dev_status, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvc

@@ -1,0 +1,93 @@
+// kvc_internal.h -- launch interface between the validating host layer
+// (kvc_host.cu) and the kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+#include "kvc.h"
+
+namespace kvc {
+
+// Segment tables travel to the kernels as launch parameters, so a call needs
+// no device allocation and concurrent calls on different streams cannot race
+// on a shared table.
+constexpr int kMaxSegments = 1024;
+
+// Wall-clock limit of every device-side wait (mbarrier, bulk copy).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+struct SegTable {
+  int32_t S;
+  int32_t req[kMaxSegments];
+  int32_t start[kMaxSegments];
+  int32_t len[kMaxSegments];
+};
+
+struct Dims {
+  int32_t R, T, L, H, d, S, Tmax, A, r;
+  int64_t units() const { return static_cast<int64_t>(S) * L * H; }
+};
+
+// Element-strided cache view (device pointer).
+struct View {
+  void* base;
+  int64_t s_req, s_layer, s_head, s_tok;
+};
+
+inline View to_view(const kvc_cache_view& v) {
+  return View{v.base, v.s_req, v.s_layer, v.s_head, v.s_tok};
+}
+
+// Device attributes cached per device by the host layer.
+struct DeviceInfo {
+  int sm_count;
+  int max_smem_optin;
+};
+cudaError_t device_info(DeviceInfo* out);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
+                         void* base, const uint64_t* dims, const uint64_t* strides_bytes,
+                         const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+// ---------------------------------------------------------------- launchers
+// K2: mean-pooled query, cosine similarities, top-k softmax weights.
+cudaError_t launch_match(const Dims& dm, const SegTable& seg, kvc_dtype dtype, const View& refK,
+                         const float* summaries, int top_k, float temperature, float* weights,
+                         int32_t* best, float* query, int32_t* dev_status, cudaStream_t stream);
+
+// K3 (bf16, tcgen05): fused correction apply + per-unit norms.
+cudaError_t launch_apply_tc(const Dims& dm, const SegTable& seg, const View refv[2],
+                            const View outv[2], const void* U[2], const void* W[2],
+                            const float* weights, float* partial, int32_t* dev_status,
+                            cudaStream_t stream);
+
+// K3 (f32, FP32 FMA): fused correction apply + per-unit norms.
+cudaError_t launch_apply_simt(const Dims& dm, const SegTable& seg, const View refv[2],
+                              const View outv[2], const void* U[2], const void* W[2],
+                              const float* weights, float* partial, cudaStream_t stream);
+
+// K4: deterministic per-segment reduction of the per-unit norms, score and flag.
+cudaError_t launch_segment_reduce(const Dims& dm, const float* partial, float tau, float* score,
+                                  uint8_t* fallback, cudaStream_t stream);
+
+// Bit-exact copy of the dense rows of every flagged segment into out.
+cudaError_t launch_fallback_copy(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
+                                 const View densev[2], const View outv[2],
+                                 const uint8_t* fallback, cudaStream_t stream);
+
+// K1: randomized low-rank delta states.
+size_t build_workspace_bytes(const Dims& dm, int l);
+cudaError_t launch_build(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
+                         const View exactv[2], const View refv[2], const float* omega, int l,
+                         int q, float energy_frac, int slot, void* U[2], void* W[2],
+                         float* sigma, int32_t* eff_rank, void* workspace, int32_t* dev_status,
+                         cudaStream_t stream);
+
+// Bounded-wait self test.
+cudaError_t launch_selftest_wait(int32_t max_polls, int32_t* dev_status, cudaStream_t stream);
+
+}  // namespace kvc

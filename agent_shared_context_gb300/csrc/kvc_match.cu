@@ -1,0 +1,200 @@
+// kvc_match.cu -- K2: match the held cache to a segment's anchors and turn
+// the similarities into weights (KVCMAS listing, Figure 1(b)).
+//
+// One CTA per unit (segment, layer, KV head).  The CTA streams the segment's
+// key rows once with 16-byte loads (HBM-bound: L*H*d*e bytes per token),
+// accumulates the column sums in fp32 in a fixed order, and then, for the
+// A <= 32 anchors, computes cosine similarities against the fp32 summaries,
+// the top_k set ordered by (-sim, index), softmax(sim / temperature) over it
+// and the argmax.  All reductions have a fixed order, so results are
+// bit-reproducible run to run.
+#include <cuda_bf16.h>
+
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+constexpr int kMatchThreads = 256;
+
+struct MatchArgs {
+  const char* ref;                // K cache base
+  int64_t s_req, s_layer, s_head, s_tok;
+  const float* summaries;         // [S, L, H, A, d]
+  float* weights;                 // [S, L, H, A]
+  int32_t* best;                  // [S, L, H]
+  float* query;                   // [S, L, H, d] or nullptr
+  int32_t L, H, d, A, top_k;
+  float inv_temperature;
+};
+
+__device__ __forceinline__ void add_vec(float (&acc)[8], const uint4& v, __nv_bfloat16) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(p[i]);
+    acc[2 * i] += f.x;
+    acc[2 * i + 1] += f.y;
+  }
+}
+
+__device__ __forceinline__ void add_vec(float (&acc)[8], const uint4& v, float) {
+  const float* p = reinterpret_cast<const float*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] += p[i];
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kMatchThreads)
+    match_kernel(const MatchArgs a, const __grid_constant__ SegTable seg) {
+  constexpr int VEC = 16 / sizeof(T);            // elements per 16-byte load
+  extern __shared__ float msm[];                 // [NG][d] partial sums, then q[d]
+  __shared__ float sims[32];
+
+  const int unit = blockIdx.x;
+  const int h = unit % a.H;
+  const int l = (unit / a.H) % a.L;
+  const int s = unit / (a.H * a.L);
+  const int n = seg.len[s];
+  const int nch = a.d / VEC;                     // 16-byte chunks per row
+  const int ng = kMatchThreads / nch;            // row groups
+  const int tid = threadIdx.x;
+  const int c = tid % nch;
+  const int g = tid / nch;
+
+  const char* base = a.ref + (static_cast<int64_t>(seg.req[s]) * a.s_req +
+                              static_cast<int64_t>(l) * a.s_layer +
+                              static_cast<int64_t>(h) * a.s_head +
+                              static_cast<int64_t>(seg.start[s]) * a.s_tok) *
+                                 static_cast<int64_t>(sizeof(T));
+  const int64_t row_bytes = a.s_tok * static_cast<int64_t>(sizeof(T));
+
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (g < ng) {
+    const char* p = base + static_cast<int64_t>(c) * 16;
+    int t = g;
+    // four independent 16-byte loads in flight per thread, consumed in row order
+    for (; t + 3 * ng < n; t += 4 * ng) {
+      const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(p + (t)*row_bytes));
+      const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(p + (t + ng) * row_bytes));
+      const uint4 v2 = __ldg(reinterpret_cast<const uint4*>(p + (t + 2 * ng) * row_bytes));
+      const uint4 v3 = __ldg(reinterpret_cast<const uint4*>(p + (t + 3 * ng) * row_bytes));
+      add_vec(acc, v0, T());
+      add_vec(acc, v1, T());
+      add_vec(acc, v2, T());
+      add_vec(acc, v3, T());
+    }
+    for (; t < n; t += ng) {
+      const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(p + t * row_bytes));
+      add_vec(acc, v0, T());
+    }
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) msm[g * a.d + c * VEC + i] = acc[i];
+  }
+  __syncthreads();
+  // fixed-order sum over row groups -> mean
+  const float inv_n = 1.0f / static_cast<float>(n);
+  float* q = msm + ng * a.d;
+  for (int j = tid; j < a.d; j += kMatchThreads) {
+    float v = 0.0f;
+    for (int gg = 0; gg < ng; ++gg) v += msm[gg * a.d + j];
+    q[j] = v * inv_n;
+  }
+  __syncthreads();
+
+  const int warp = tid >> 5, lane = tid & 31;
+  const int64_t uoff = static_cast<int64_t>(unit);
+  if (a.query != nullptr) {
+    for (int j = tid; j < a.d; j += kMatchThreads) a.query[uoff * a.d + j] = q[j];
+  }
+  // |q|^2 by warp 0 (fixed order)
+  __shared__ float qq_sh;
+  if (warp == 0) {
+    float v = 0.0f;
+    for (int j = lane; j < a.d; j += 32) v += q[j] * q[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) qq_sh = v;
+  }
+  __syncthreads();
+  const float qn = sqrtf(qq_sh);
+  const float* sbase = a.summaries + uoff * a.A * a.d;
+  // per-anchor dot products: warp w handles anchors w, w+8, ...
+  for (int an = warp; an < a.A; an += kMatchThreads / 32) {
+    float dot = 0.0f, ss = 0.0f;
+    for (int j = lane; j < a.d; j += 32) {
+      const float sv = __ldg(sbase + an * a.d + j);
+      dot += q[j] * sv;
+      ss += sv * sv;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    }
+    if (lane == 0) {
+      const float sn = sqrtf(ss);
+      sims[an] = (qn == 0.0f || sn == 0.0f) ? 0.0f : dot / (qn * sn);
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const bool valid = lane < a.A;
+    const float sim = valid ? sims[lane] : -INFINITY;
+    int rank = 0;
+    for (int b = 0; b < a.A; ++b) {
+      const float sb = sims[b];
+      rank += (sb > sim || (sb == sim && b < lane)) ? 1 : 0;
+    }
+    const bool kept = valid && rank < a.top_k;
+    // the maximum similarity sits at rank 0
+    const unsigned is_best = __ballot_sync(0xffffffffu, valid && rank == 0);
+    const int best_idx = __ffs(is_best) - 1;
+    const float top = sims[best_idx];
+    float e = kept ? expf((sim - top) * a.inv_temperature) : 0.0f;
+    float den = e;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (valid) a.weights[uoff * a.A + lane] = kept ? e / den : 0.0f;
+    if (lane == 0) a.best[uoff] = best_idx;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_match(const Dims& dm, const SegTable& seg, kvc_dtype dtype, const View& refK,
+                         const float* summaries, int top_k, float temperature, float* weights,
+                         int32_t* best, float* query, int32_t* dev_status, cudaStream_t stream) {
+  (void)dev_status;
+  MatchArgs a{};
+  a.ref = static_cast<const char*>(refK.base);
+  a.s_req = refK.s_req;
+  a.s_layer = refK.s_layer;
+  a.s_head = refK.s_head;
+  a.s_tok = refK.s_tok;
+  a.summaries = summaries;
+  a.weights = weights;
+  a.best = best;
+  a.query = query;
+  a.L = dm.L;
+  a.H = dm.H;
+  a.d = dm.d;
+  a.A = dm.A;
+  a.top_k = top_k;
+  a.inv_temperature = 1.0f / temperature;
+  const int64_t units = dm.units();
+  if (units <= 0) return cudaSuccess;
+  if (units > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const int vec = dtype == KVC_BF16 ? 8 : 4;
+  const int nch = dm.d / vec;
+  const int ng = kMatchThreads / nch;
+  const size_t smem = static_cast<size_t>(ng + 1) * dm.d * sizeof(float);
+  if (dtype == KVC_BF16) {
+    match_kernel<__nv_bfloat16><<<static_cast<unsigned>(units), kMatchThreads, smem, stream>>>(a, seg);
+  } else {
+    match_kernel<float><<<static_cast<unsigned>(units), kMatchThreads, smem, stream>>>(a, seg);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvc
