@@ -1,0 +1,186 @@
+"""GPU parity of the state builder (kvc_build_states) against the oracle.
+
+The factors of a truncated SVD carry sign / rotation freedom, so parity is on
+the product U W^T per (segment, layer, head, K|V) block, which is unique
+whenever sigma_r > sigma_{r+1} of the sketch.  Effective ranks are integers
+and compared exactly wherever the oracle's cumulative energy fraction is at
+least 1e-3 away from energy_frac at the deciding index (otherwise either
+neighbouring rank is a valid answer).  Tolerances: f32 relative Frobenius
+error of U W^T <= 1e-4; bf16 <= 2e-2 (the builder runs in fp32 on the exact
+fp32 difference of the bf16 inputs; the stored U and W are rounded to bf16,
+~2^-9 each).
+"""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from agent_shared_context_gb300 import synth
+
+from ._harness import check_out, np64, oracle_chain
+
+pytestmark = pytest.mark.gpu
+
+
+def _kvc():
+    from agent_shared_context_gb300 import kvc
+    return kvc
+
+
+def _cases():
+    tiny = synth.workload("tiny")
+    LC = synth.workload("longctx")
+    return {
+        "tiny-f32": tiny,
+        "tiny-noise-free": dataclasses.replace(tiny, noise=0.0),
+        "longctx-small": synth.scaled(LC, L=1, H=2, R=1, seg_len=[256, 256, 200],
+                                      fallback_frac=0.34),
+        "d64-bf16": synth.scaled(LC, L=1, H=2, R=1, seg_len=[300, 64], d=64, A=4, r=24,
+                                 oversample=8, fallback_frac=0.0),
+    }
+
+
+def _margin_ok(sig, total, frac, k):
+    """True when the effective-rank decision at k is >= 1e-3 from the boundary."""
+    if total <= 0:
+        return True
+    cum = np.cumsum(np.asarray(sig, np.float64) ** 2) / total
+    ok = True
+    if 1 <= k <= len(cum):
+        ok &= abs(cum[k - 1] - frac) >= 1e-3
+    if 2 <= k <= len(cum) + 1:
+        ok &= abs(cum[k - 2] - frac) >= 1e-3
+    return ok
+
+
+@pytest.mark.parametrize("name", list(_cases().keys()))
+def test_build_states_matches_oracle(name):
+    kvc = _kvc()
+    wl = _cases()[name]
+    if wl.build_slot < 0:
+        wl = dataclasses.replace(wl, build_slot=0)
+    inp = synth.generate(wl, device="cuda", edges=[1])
+    e = inp.edges[0]
+    seg = kvc.Segments.from_workload(wl)
+    prm = kvc.params_from_workload(wl)
+    S, L, H, l = wl.S, wl.L, wl.H, wl.l
+    sigma = torch.full((S, L, H, 2, l), -1.0, device="cuda")
+    erank = torch.full((S, L, H, 2), -7, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(kvc.kvc_build_states_workspace(seg, prm), 256), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    U_K, W_K, U_V, W_V = (x.clone() for x in (e.U_K, e.W_K, e.U_V, e.W_V))
+    slot = 1 % wl.A
+    kvc.kvc_build_states(seg, prm, inp.exact_K[1], inp.exact_V[1], inp.exact_K[0],
+                         inp.exact_V[0], inp.omega, slot, U_K, W_K, U_V, W_V, sigma, erank, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # other slots untouched
+    others = [a for a in range(wl.A) if a != slot]
+    if others:
+        assert torch.equal(U_K[:, :, :, :, others], e.U_K[:, :, :, :, others])
+        assert torch.equal(W_V[:, :, :, :, others], e.W_V[:, :, :, :, others])
+    om = np64(inp.omega)
+    EK = [np64(t) for t in inp.exact_K]
+    EV = [np64(t) for t in inp.exact_V]
+    tol = 1e-4 if wl.dtype == "f32" else 2e-2
+    worst = 0.0
+    for s in range(S):
+        q, t0, n = wl.seg_request[s], wl.seg_start[s], wl.seg_len[s]
+        for layer in range(L):
+            for h in range(H):
+                for kv, (E1, E0, Ug, Wg) in enumerate(((EK[1], EK[0], U_K, W_K),
+                                                        (EV[1], EV[0], U_V, W_V))):
+                    Uo, Wo, svo, ero = O.build_unit(E1[q, layer, h, t0:t0 + n], E0[q, layer, h, t0:t0 + n],
+                                                    wl.r, om, wl.power_iters, wl.energy_frac)
+                    ug = np64(Ug[s, layer, h, :, slot, :])
+                    wg = np64(Wg[s, layer, h, :, slot, :])
+                    assert np.all(ug[n:] == 0)              # rows beyond the segment zeroed
+                    prod_o = Uo @ Wo.T
+                    prod_g = ug[:n] @ wg.T
+                    rel = O.relative_error(prod_g, prod_o)
+                    worst = max(worst, rel)
+                    assert rel <= tol, (s, layer, h, kv, rel)
+                    sg = sigma[s, layer, h, kv].cpu().numpy()
+                    np.testing.assert_allclose(sg[:wl.r], svo[:wl.r], rtol=10 * tol,
+                                               atol=1e-5 * svo[0])
+                    delta = E1[q, layer, h, t0:t0 + n] - E0[q, layer, h, t0:t0 + n]
+                    total = float(np.sum(delta * delta))
+                    if _margin_ok(svo, total, wl.energy_frac, ero):
+                        assert int(erank[s, layer, h, kv]) == ero, (s, layer, h, kv)
+    print("%s: worst relative error of U W^T %.2e" % (name, worst))
+
+
+def test_build_noise_free_planted_rank4_reconstructs_delta():
+    """The pinned special case on the GPU: planted rank-4 delta, r = 8."""
+    kvc = _kvc()
+    wl = dataclasses.replace(synth.workload("tiny"), noise=0.0)
+    inp = synth.generate(wl, device="cuda", edges=[1])
+    e = inp.edges[0]
+    seg = kvc.Segments.from_workload(wl)
+    prm = kvc.params_from_workload(wl)
+    sigma = torch.empty((1, 1, 2, 2, wl.l), device="cuda")
+    erank = torch.empty((1, 1, 2, 2), dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(kvc.kvc_build_states_workspace(seg, prm), 256), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvc.kvc_build_states(seg, prm, inp.exact_K[1], inp.exact_V[1], inp.exact_K[0], inp.exact_V[0],
+                         inp.omega, 0, e.U_K, e.W_K, e.U_V, e.W_V, sigma, erank, ws, st)
+    torch.cuda.synchronize()
+    for kv, (E1, E0, U, W) in enumerate(((inp.exact_K[1], inp.exact_K[0], e.U_K, e.W_K),
+                                          (inp.exact_V[1], inp.exact_V[0], e.U_V, e.W_V))):
+        for h in range(2):
+            delta = np64(E1[0, 0, h]) - np64(E0[0, 0, h])
+            prod = np64(U[0, 0, h, :, 0, :]) @ np64(W[0, 0, h, :, 0, :]).T
+            assert O.relative_error(prod, delta) < 1e-5
+            # singular values 2, 1, 0.5, 0.25 -> energies 4, 1, .25, .0625: rank 2
+            assert int(erank[0, 0, h, kv]) == 2
+            np.testing.assert_allclose(sigma[0, 0, h, kv, :4].cpu().numpy(), [2, 1, 0.5, 0.25],
+                                       rtol=1e-4)
+
+
+@pytest.mark.parametrize("name", ["tiny-f32", "longctx-small"])
+def test_chain_with_builder_matches_oracle(name):
+    """Chain in which every edge first rebuilds slot 0 from exact_j - held_{j-1}."""
+    from agent_shared_context_gb300.chain import ChainRunner
+    wl = _cases()[name]
+    inp = synth.generate(wl, device="cuda")
+    runner = ChainRunner(wl, inp, device="cuda", poison_ph=True, build=True)
+    # the runner writes built states into the edge inputs; keep the originals for the oracle
+    orig = [dataclasses.replace(e, U_K=e.U_K.clone(), W_K=e.W_K.clone(), U_V=e.U_V.clone(),
+                                W_V=e.W_V.clone()) for e in inp.edges]
+    runner.run()
+    torch.cuda.synchronize()
+    assert int(runner.dev_status.item()) == 0
+    inp_o = dataclasses.replace(inp, edges=orig)
+    res, _ = oracle_chain(wl, inp_o, build=True)
+    bf16 = wl.dtype == "bf16"
+    for j in range(1, wl.edges + 1):
+        eo = runner.edges[j]
+        fb = eo.fallback.cpu().numpy().astype(bool)
+        assert np.array_equal(fb, res[j]["fallback"]), (j, fb, res[j]["score"])
+        # the built slot differs from the oracle's by the builder tolerance, which
+        # enters C linearly through its weight: allow 2e-2 of |C| on top of rounding
+        for kv, key in ((0, "out_K"), (1, "out_V")):
+            out_g = np64(getattr(eo, key))
+            out_o = res[j][key]
+            ref_o = res[j - 1][key]
+            for s in range(wl.S):
+                if fb[s]:
+                    continue
+                q, t0, n = wl.seg_request[s], wl.seg_start[s], wl.seg_len[s]
+                for layer in range(wl.L):
+                    for h in range(wl.H):
+                        g = out_g[q, layer, h, t0:t0 + n]
+                        o = out_o[q, layer, h, t0:t0 + n]
+                        c = np.linalg.norm(o - ref_o[q, layer, h, t0:t0 + n])
+                        err = np.linalg.norm(g - o)
+                        bound = (2e-2 if bf16 else 1e-4) * c + (j * 2.0 ** -8 if bf16 else 1e-6) * np.linalg.norm(o)
+                        assert err <= bound, (j, s, layer, h, err, c)
+        er_g = eo.eff_rank.cpu().numpy()
+        er_o = res[j]["eff_rank"]
+        agree = float(np.mean(er_g == er_o))
+        assert agree >= 0.9, (j, er_g, er_o)
