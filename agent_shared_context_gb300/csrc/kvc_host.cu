@@ -196,6 +196,10 @@ kvc_status check_apply_args(const kvc_segments* seg, const kvc_cache_view& ref_K
 
 }  // namespace
 
+kvc_status set_last_error(kvc_status st, const char* msg) {
+  return fail(st, "%s", msg);
+}
+
 // ------------------------------------------------------------ device info
 cudaError_t device_info(DeviceInfo* out) {
   static std::mutex mu;

@@ -41,6 +41,9 @@ inline View to_view(const kvc_cache_view& v) {
   return View{v.base, v.s_req, v.s_layer, v.s_head, v.s_tok};
 }
 
+// Records `msg` as this thread's last error message and returns `st`.
+kvc_status set_last_error(kvc_status st, const char* msg);
+
 // Device attributes cached per device by the host layer.
 struct DeviceInfo {
   int sm_count;

@@ -44,7 +44,9 @@ KVC_F32 = 1
 EXPORTS = ("kvc_version", "kvc_status_string", "kvc_last_error",
            "kvc_build_states_workspace", "kvc_build_states", "kvc_match_anchors",
            "kvc_apply_correction", "kvc_chain_edge_workspace", "kvc_chain_edge",
-           "kvc_selftest_bounded_wait")
+           "kvc_selftest_bounded_wait", "kvc_chain_edge_noalloc")
+
+KVC_NOALLOC_MAX_UNITS = 262144
 
 
 class KvcError(RuntimeError):
@@ -103,6 +105,10 @@ lib.kvc_chain_edge.restype = _ST
 lib.kvc_chain_edge.argtypes = [ctypes.c_int32, _SEG_P, _PRM_P, _VIEW, _VIEW, _VP, _VP, _VP, _VP,
                                _VP, _VIEW, _VIEW, _VIEW, _VIEW, _VP, _VP, _VP, _VP, _VP,
                                ctypes.c_size_t, _VP, _VP]
+lib.kvc_chain_edge_noalloc.restype = _ST
+lib.kvc_chain_edge_noalloc.argtypes = [ctypes.c_int32, _SEG_P, _PRM_P, _VIEW, _VIEW, _VP, _VP, _VP,
+                                       _VP, _VP, _VIEW, _VIEW, _VIEW, _VIEW, _VP, _VP, _VP, _VP,
+                                       _VP, _VP]
 lib.kvc_selftest_bounded_wait.restype = _ST
 lib.kvc_selftest_bounded_wait.argtypes = [ctypes.c_int32, _VP, _VP]
 
@@ -258,6 +264,22 @@ def kvc_chain_edge(edge: int, seg: Segments, prm: kvc_params, ref_K, ref_V, summ
                             _addr(best), _addr(score), _addr(fallback), _addr(workspace),
                             ws_bytes, _addr(dev_status), _stream(stream))
     return _done(st, "kvc_chain_edge", check)
+
+
+def kvc_chain_edge_noalloc(edge: int, seg: Segments, prm: kvc_params, ref_K, ref_V,
+                           summaries: Ptr, U_K: Ptr, W_K: Ptr, U_V: Ptr, W_V: Ptr, dense_K,
+                           dense_V, out_K, out_V, weights: Ptr, best: Ptr, score: Ptr,
+                           fallback: Ptr, dev_status: Ptr, stream=None, check: bool = True) -> int:
+    """kvc_chain_edge without a workspace argument, for callers that cannot
+    allocate device memory (the library's own device scratch array is used;
+    include/kvc.h states its size limit and the rule that overlapping calls
+    on one device race)."""
+    st = lib.kvc_chain_edge_noalloc(int(edge), seg.ref, ctypes.byref(prm), _v(ref_K), _v(ref_V),
+                                    _addr(summaries), _addr(U_K), _addr(W_K), _addr(U_V),
+                                    _addr(W_V), _v(dense_K), _v(dense_V), _v(out_K), _v(out_V),
+                                    _addr(weights), _addr(best), _addr(score), _addr(fallback),
+                                    _addr(dev_status), _stream(stream))
+    return _done(st, "kvc_chain_edge_noalloc", check)
 
 
 def kvc_selftest_bounded_wait(max_polls: int, dev_status: Ptr, stream=None,

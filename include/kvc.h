@@ -238,6 +238,42 @@ kvc_status kvc_chain_edge(int32_t edge, const kvc_segments* seg, const kvc_param
                           int32_t* dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * kvc_chain_edge_noalloc -- kvc_chain_edge for callers that cannot allocate
+ * device memory.  The paper has no counterpart: this is a library service.
+ *
+ * Some callers cannot call cudaMalloc: a plugin inside a host application
+ * whose memory manager owns all of the GPU's memory and exposes no
+ * allocation hook, or a serving loop that forbids allocation on the request
+ * path because cudaMalloc/cudaFree can synchronise the device.  This variant
+ * takes the per-unit norm scratch from a 4 MiB device array inside the
+ * library (created when the library's device code is loaded, held until
+ * process exit) instead of a caller workspace; every input and output is
+ * still the caller's.  It allocates nothing and otherwise behaves exactly
+ * like kvc_chain_edge (same arguments minus the workspace, same results).
+ *
+ * Limits and rules:
+ *   - S * L * H must not exceed KVC_NOALLOC_MAX_UNITS, else the call returns
+ *     KVC_ERR_WORKSPACE with a message, before anything is launched;
+ *   - the first call on a device (any edge) looks up the array's device
+ *     address for that device; make that first call before any stream
+ *     capture;
+ *   - all calls on a device share the array: calls whose work may overlap on
+ *     the GPU (unordered streams) race on it and must be serialised by the
+ *     caller.  Each call writes every scratch entry it reads, so nothing needs
+ *     clearing between calls.
+ * ------------------------------------------------------------------------- */
+#define KVC_NOALLOC_MAX_UNITS 262144
+kvc_status kvc_chain_edge_noalloc(int32_t edge, const kvc_segments* seg, const kvc_params* prm,
+                                  kvc_cache_view ref_K, kvc_cache_view ref_V,
+                                  const float* summaries,
+                                  const void* U_K, const void* W_K,
+                                  const void* U_V, const void* W_V,
+                                  kvc_cache_view dense_K, kvc_cache_view dense_V,
+                                  kvc_cache_view out_K, kvc_cache_view out_V,
+                                  float* weights, int32_t* best, float* score, uint8_t* fallback,
+                                  int32_t* dev_status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * kvc_selftest_bounded_wait -- launches one CTA that waits on an mbarrier no
  * one arrives on, giving up after `max_polls` polls; it then stores
  * KVC_ERR_DEVICE_TIMEOUT into *dev_status and returns.  Exercises the
