@@ -162,6 +162,24 @@ __global__ void __launch_bounds__(kRedThreads)
   }
 }
 
+// ---------------------------------------------------- reuse-ratio select
+// Reuse-ratio mode (listing, Figure 5 and Tables 11-12 fix rho directly):
+// one CTA ranks the S <= 1024 segment scores by (-score, index) and flags
+// the first S - n_reuse of them for fallback.
+__global__ void __launch_bounds__(1024)
+    select_ratio_kernel(const float* __restrict__ score, int S, int n_reuse,
+                        uint8_t* __restrict__ fallback) {
+  __shared__ float sc[kMaxSegments];
+  for (int s = threadIdx.x; s < S; s += blockDim.x) sc[s] = score[s];
+  __syncthreads();
+  for (int s = threadIdx.x; s < S; s += blockDim.x) {
+    const float v = sc[s];
+    int rank = 0;
+    for (int t = 0; t < S; ++t) rank += (sc[t] > v || (sc[t] == v && t < s)) ? 1 : 0;
+    fallback[s] = rank < S - n_reuse ? 1 : 0;
+  }
+}
+
 // -------------------------------------------------------- fallback copy
 struct CopyArgs {
   const char* src[2];
@@ -189,7 +207,25 @@ __global__ void __launch_bounds__(256)
                            static_cast<int64_t>(seg.start[s]) * a.ds[kv][3]) * e;
   const int vec_per_row = a.row_bytes / 16;
   const int total = seg.len[s] * vec_per_row;
-  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+  const int step = blockDim.x;
+  // four independent 16-byte loads in flight per thread
+  int i = threadIdx.x;
+  for (; i + 3 * step < total; i += 4 * step) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = i + u * step;
+      const int t = k / vec_per_row, c = k % vec_per_row;
+      v[u] = __ldg(reinterpret_cast<const uint4*>(src + t * a.ss[kv][3] * e) + c);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = i + u * step;
+      const int t = k / vec_per_row, c = k % vec_per_row;
+      reinterpret_cast<uint4*>(dst + t * a.ds[kv][3] * e)[c] = v[u];
+    }
+  }
+  for (; i < total; i += step) {
     const int t = i / vec_per_row, c = i % vec_per_row;
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + t * a.ss[kv][3] * e) + c);
     reinterpret_cast<uint4*>(dst + t * a.ds[kv][3] * e)[c] = v;
@@ -251,6 +287,13 @@ cudaError_t launch_segment_reduce(const Dims& dm, const float* partial, float ta
   if (dm.S <= 0) return cudaSuccess;
   segment_reduce_kernel<<<dm.S, kRedThreads, 0, stream>>>(partial, dm.L * dm.H, tau, score,
                                                           fallback);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select_ratio(const Dims& dm, const float* score, int n_reuse,
+                                uint8_t* fallback, cudaStream_t stream) {
+  if (dm.S <= 0) return cudaSuccess;
+  select_ratio_kernel<<<1, 1024, 0, stream>>>(score, dm.S, n_reuse, fallback);
   return cudaGetLastError();
 }
 

@@ -6,9 +6,11 @@
 // is the skinny product C[n, d] = U[n, A*r] . (w (.) W)[A*r, d]^T, where the
 // anchor weights are folded into W once per item.  Per 128-token tile:
 //
-//   warp 0 (1 thread)  TMA: the item's W chunks (once), the ref tile and the
-//                      U chunks (64 columns = one 128-byte swizzle row each)
-//                      into shared-memory rings guarded by mbarriers;
+//   warp 0 (1 thread)  TMA: the item's W chunks (once) and the U chunks (64
+//                      columns = one 128-byte swizzle row each) into a
+//                      shared-memory ring guarded by mbarriers;
+//   warp 6 (1 thread)  TMA: the ref tiles into their own ring, so U
+//                      prefetch never waits for a ref buffer;
 //   warp 1 (1 thread)  tcgen05.mma kind::f16, M = 128 tokens, N = d,
 //                      K = A*r in steps of 16, accumulating in TMEM (two
 //                      accumulator buffers so tile t+1's MMAs overlap tile
@@ -43,9 +45,9 @@ using namespace ptx;
 constexpr int kBM = 128;                   // tokens per tile (MMA M)
 constexpr int kChunk = 64;                 // bf16 per 128-byte swizzled row
 constexpr int kUStageBytes = kBM * 128;    // one U chunk: 128 rows x 128 B
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kMaxUStages = 8;
-constexpr int kMaxRefBufs = 2;
+constexpr int kMaxRefBufs = 3;
 constexpr int kEpiThreads = 128;
 
 struct TcMaps {
@@ -71,7 +73,7 @@ struct Bars {
   uint64_t ref_full[kMaxRefBufs], ref_empty[kMaxRefBufs];
   uint32_t tmem_base;
   int32_t abort_flag;
-  int32_t epi_ok;
+  int32_t epi_ok[2];
   float red[2][4];
 };
 
@@ -162,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->ref_empty[i], 1);
     }
     bars->abort_flag = 0;
-    bars->epi_ok = 1;
+    bars->epi_ok[0] = 1;
+    bars->epi_ok[1] = 1;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -183,11 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&maps.W[kv]);
         tma_prefetch_desc(&maps.out[kv]);
       }
-      uint32_t ust = 0, uph = 0, rb = 0, rph = 0, wfree_ph = 0;
-      uint32_t u_last[kMaxUStages], r_last[kMaxRefBufs];
-      bool u_used[kMaxUStages], r_used[kMaxRefBufs];
+      uint32_t ust = 0, uph = 0, wfree_ph = 0;
+      uint32_t u_last[kMaxUStages];
+      bool u_used[kMaxUStages];
       for (int i = 0; i < kMaxUStages; ++i) u_used[i] = false;
-      for (int i = 0; i < kMaxRefBufs; ++i) r_used[i] = false;
       bool w_used = false;
       uint32_t w_last = 0, w_issue_count = 0;
       bool ok = true;
@@ -213,21 +215,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           w_issued = true;
         };
         for (int t = 0; t < x.ntiles && ok; ++t) {
-          if (!wait_or_abort(&bars->ref_empty[rb], rph ^ 1u, bars, a.dev_status)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&bars->ref_full[rb], static_cast<uint32_t>(REFB));
-#pragma unroll
-          for (int sub = 0; sub < NSUB; ++sub)
-            tma_load_5d(r_smem + rb * REFB + sub * (kBM * 128), &maps.ref[x.kv],
-                        &bars->ref_full[rb], sub * kChunk, x.start + t * kBM, x.h, x.l, x.req);
-          r_last[rb] = rph;
-          r_used[rb] = true;
-          if (++rb == static_cast<uint32_t>(NRB)) {
-            rb = 0;
-            rph ^= 1u;
-          }
           for (int kc = 0; kc < a.KC; ++kc) {
             if (!w_issued && uc == w_after) {
               issue_w();
@@ -255,9 +242,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       // before the CTA may exit (bounded; a no-op after normal completion).
       for (int i = 0; i < NSU; ++i)
         if (u_used[i]) (void)mbar_wait_bounded(&bars->u_full[i], u_last[i], kWaitLimitNs);
+      if (w_used) (void)mbar_wait_bounded(&bars->w_full, w_last, kWaitLimitNs);
+    }
+  } else if (warp == 6) {
+    // -------------------------------------------------------- ref producer
+    if (lane == 0) {
+      uint32_t rb = 0, rph = 0;
+      uint32_t r_last[kMaxRefBufs];
+      bool r_used[kMaxRefBufs];
+      for (int i = 0; i < kMaxRefBufs; ++i) r_used[i] = false;
+      bool ok = true;
+      for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x) {
+        const Item x = decode_item(it, a, seg);
+        for (int t = 0; t < x.ntiles; ++t) {
+          if (!wait_or_abort(&bars->ref_empty[rb], rph ^ 1u, bars, a.dev_status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->ref_full[rb], static_cast<uint32_t>(REFB));
+#pragma unroll
+          for (int sub = 0; sub < NSUB; ++sub)
+            tma_load_5d(r_smem + rb * REFB + sub * (kBM * 128), &maps.ref[x.kv],
+                        &bars->ref_full[rb], sub * kChunk, x.start + t * kBM, x.h, x.l, x.req);
+          r_last[rb] = rph;
+          r_used[rb] = true;
+          if (++rb == static_cast<uint32_t>(NRB)) {
+            rb = 0;
+            rph ^= 1u;
+          }
+        }
+      }
       for (int i = 0; i < NRB; ++i)
         if (r_used[i]) (void)mbar_wait_bounded(&bars->ref_full[i], r_last[i], kWaitLimitNs);
-      if (w_used) (void)mbar_wait_bounded(&bars->w_full, w_last, kWaitLimitNs);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -325,18 +341,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m = q * 32 + lane;              // token row of the tile
     uint32_t wf_ph = 0, rph = 0, rb = 0, tile_count = 0;
     uint32_t acc_fph[2] = {0u, 0u};
-    volatile int32_t* epi_ok = &bars->epi_ok;
-    // One thread waits (bounded) and broadcasts the outcome; the others then
-    // re-check the completed phase, which returns at once and orders their
-    // reads after the producer's writes.
+    uint32_t n_waits = 0;
+    // One thread waits (bounded) and broadcasts the outcome through one of
+    // two flag slots (a slot is rewritten only two waits later, after every
+    // thread has passed the intervening barrier); the others then re-check
+    // the completed phase, which returns at once and orders their reads
+    // after the producer's writes.
     auto epi_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      if (et == 0) *epi_ok = wait_or_abort(bar, parity, bars, a.dev_status) ? 1 : 0;
+      volatile int32_t* slot = &bars->epi_ok[n_waits & 1u];
+      ++n_waits;
+      if (et == 0) *slot = wait_or_abort(bar, parity, bars, a.dev_status) ? 1 : 0;
       named_sync(1, kEpiThreads);
-      const bool ok = *epi_ok != 0;
+      const bool ok = *slot != 0;
       if (ok && et != 0) (void)mbar_wait_bounded(bar, parity, kWaitLimitNs);
-      named_sync(1, kEpiThreads);
       return ok;
     };
+    // With three or more ref buffers the thread that issues a tile's TMA
+    // store releases its buffer one tile later, once the store has finished
+    // reading shared memory, instead of waiting for it on the spot.
+    const bool defer_release = NRB >= 3;
+    int pending_rb = -1;
     for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
       const Item x = decode_item(it, a, seg);
       if (!epi_wait(&bars->w_full, wf_ph)) break;
@@ -381,16 +405,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* rt = r_smem + rb * REFB;
         const bool row_ok = m < rows_valid;
 #pragma unroll 1
-        for (int cb = 0; cb < D / 16; ++cb) {
-          uint32_t v[16];
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t v[32];
           __syncwarp();
-          tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(q * 32) << 16) + b * D + cb * 16, v);
+          const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * D + cb * 32;
+          tmem_ld_32x32b_x16(ta, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+          tmem_ld_32x32b_x16(ta + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
           tmem_ld_wait();
-          const int col0 = cb * 16;
+          const int col0 = cb * 32;
           const int sub = col0 / kChunk;
           const int j0 = (col0 % kChunk) / 8;
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
+          for (int u = 0; u < 4; ++u) {
             const int j = j0 + u;
             uint4* p = reinterpret_cast<uint4*>(rt + sub * (kBM * 128) + m * 128 +
                                                 ((j ^ (m & 7)) << 4));
@@ -423,8 +449,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_store_5d(&maps.out[x.kv], rt + sub * (kBM * 128), sub * kChunk,
                            x.start + t * kBM, x.h, x.l, x.req);
             bulk_commit_group();
-            bulk_wait_group_read<0>();
-            mbar_arrive(&bars->ref_empty[rb]);
+            if (defer_release) {
+              if (pending_rb >= 0) {
+                bulk_wait_group_read<1>();          // the previous store is done reading
+                mbar_arrive(&bars->ref_empty[pending_rb]);
+              }
+              pending_rb = static_cast<int>(rb);
+            } else {
+              bulk_wait_group_read<0>();
+              mbar_arrive(&bars->ref_empty[rb]);
+            }
           }
         } else {
           if (row_ok) {
@@ -444,7 +478,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           named_sync(1, kEpiThreads);
-          if (et == 0) mbar_arrive(&bars->ref_empty[rb]);
+          if (et == 0) {
+            mbar_arrive(&bars->ref_empty[rb]);
+            if (pending_rb >= 0) {                 // no later store would release it
+              bulk_wait_group_read<0>();
+              mbar_arrive(&bars->ref_empty[pending_rb]);
+              pending_rb = -1;
+            }
+          }
         }
         if (++rb == static_cast<uint32_t>(NRB)) {
           rb = 0;
@@ -472,7 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       named_sync(1, kEpiThreads);
     }
-    if (et == 0) bulk_wait_group<0>();
+    if (et == 0) {
+      bulk_wait_group<0>();
+      if (pending_rb >= 0) mbar_arrive(&bars->ref_empty[pending_rb]);
+    }
   }
 
   tc_fence_before();
@@ -494,13 +538,20 @@ cudaError_t launch_d(const Dims& dm, const SegTable& seg, const View refv[2], co
   constexpr int REFB = kBM * D * 2;
   const size_t fixed = 1024 + sizeof(Bars) + 64;
   const size_t budget = static_cast<size_t>(di.max_smem_optin);
-  int nrb = 2, nsu = 0;
-  for (; nrb >= 1; --nrb) {
-    const size_t used = fixed + static_cast<size_t>(KC) * WCB + static_cast<size_t>(nrb) * REFB;
+  // Prefer three ref buffers (deferred store release) with >= 4 U stages,
+  // then two with >= 3, then one with >= 2.
+  int nrb = 0, nsu = 0;
+  const int want_nsu[4] = {0, 2, 3, 4};
+  for (int cand = kMaxRefBufs; cand >= 1; --cand) {
+    const size_t used = fixed + static_cast<size_t>(KC) * WCB + static_cast<size_t>(cand) * REFB;
     if (used >= budget) continue;
-    nsu = static_cast<int>((budget - used) / kUStageBytes);
-    if (nsu > kMaxUStages) nsu = kMaxUStages;
-    if (nsu >= 3 || (nrb == 1 && nsu >= 2)) break;
+    int n = static_cast<int>((budget - used) / kUStageBytes);
+    if (n > kMaxUStages) n = kMaxUStages;
+    if (n >= want_nsu[cand]) {
+      nrb = cand;
+      nsu = n;
+      break;
+    }
   }
   if (nrb < 1 || nsu < 2) return cudaErrorInvalidConfiguration;
   const size_t smem = fixed + static_cast<size_t>(KC) * WCB + static_cast<size_t>(nrb) * REFB +

@@ -50,6 +50,10 @@ struct BuildArgs {
   int64_t slot_floats;
   int32_t L, H, d, Tmax, A, r, l, q, slot, n_mats;
   float energy_frac;
+  // anchor-pool insertion (all nullptr for a plain build into `slot`)
+  const uint8_t* seg_mask;   // [S]: build only flagged segments
+  const int32_t* seg_slot;   // [S]: slot = seg_slot[s] mod A
+  float* summaries;          // [S, L, H, A, d]: slot summary = held key mean
 };
 
 template <typename T>
@@ -299,6 +303,8 @@ __global__ void __launch_bounds__(kBuildThreads)
     const int lyr = (unit / a.H) % a.L;
     const int s = unit / (a.H * a.L);
     const int n = seg.len[s];
+    if (a.seg_mask != nullptr && a.seg_mask[s] == 0) continue;   // uniform per CTA
+    const int slot = a.seg_slot != nullptr ? ((a.seg_slot[s] % a.A) + a.A) % a.A : a.slot;
     const T* ex = reinterpret_cast<const T*>(a.exact[kv]) + seg.req[s] * a.es[kv][0] +
                   lyr * a.es[kv][1] + h * a.es[kv][2] +
                   static_cast<int64_t>(seg.start[s]) * a.es[kv][3];
@@ -316,6 +322,15 @@ __global__ void __launch_bounds__(kBuildThreads)
       ss = fmaf(v, v, ss);
     }
     const float total = block_sum(ss, red);
+    if (a.summaries != nullptr && kv == 0) {
+      // summary of the new anchor: mean of the held keys (fixed order)
+      float* sm = a.summaries + (static_cast<int64_t>(unit) * a.A + slot) * d;
+      for (int c = threadIdx.x; c < d; c += kBuildThreads) {
+        float acc = 0.0f;
+        for (int t = 0; t < n; ++t) acc += ld_elem<T>(rf + t * a.rs[kv][3] + c);
+        sm[c] = acc / static_cast<float>(n);
+      }
+    }
     for (int idx = threadIdx.x; idx < d * l; idx += kBuildThreads) X[idx] = __ldg(a.omega + idx);
     __syncthreads();
 
@@ -373,7 +388,7 @@ __global__ void __launch_bounds__(kBuildThreads)
         for (int i = 0; i < l; ++i) acc = fmaf(qrow[i], R[i * kLMax + col], acc);
         v = acc * sj;
       }
-      st_elem<T>(Uo + (static_cast<int64_t>(t) * a.A + a.slot) * a.r + j, v);
+      st_elem<T>(Uo + (static_cast<int64_t>(t) * a.A + slot) * a.r + j, v);
     }
     // ---- W = B^T Ub_r diag(1 / sigma_r) (zero for negligible sigma)
     T* Wo = reinterpret_cast<T*>(a.W[kv]) + static_cast<int64_t>(unit) * d * a.A * a.r;
@@ -389,7 +404,7 @@ __global__ void __launch_bounds__(kBuildThreads)
           v = acc / sj;
         }
       }
-      st_elem<T>(Wo + (static_cast<int64_t>(c) * a.A + a.slot) * a.r + j, v);
+      st_elem<T>(Wo + (static_cast<int64_t>(c) * a.A + slot) * a.r + j, v);
     }
     __syncthreads();
   }
@@ -416,9 +431,13 @@ cudaError_t launch_build(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
                          const View exactv[2], const View refv[2], const float* omega, int l,
                          int q, float energy_frac, int slot, void* U[2], void* W[2],
                          float* sigma, int32_t* eff_rank, void* workspace, int32_t* dev_status,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const uint8_t* seg_mask, const int32_t* seg_slot,
+                         float* summaries) {
   (void)dev_status;
   BuildArgs a{};
+  a.seg_mask = seg_mask;
+  a.seg_slot = seg_slot;
+  a.summaries = summaries;
   for (int kv = 0; kv < 2; ++kv) {
     a.exact[kv] = static_cast<const char*>(exactv[kv].base);
     a.ref[kv] = static_cast<const char*>(refv[kv].base);
@@ -468,6 +487,21 @@ cudaError_t launch_build(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
     if (e != cudaSuccess) return e;
     build_simt_kernel<float><<<grid, kBuildThreads, smem, stream>>>(a, seg);
   }
+  return cudaGetLastError();
+}
+
+namespace {
+__global__ void pool_advance_kernel(const uint8_t* __restrict__ fallback, int32_t* pool_next,
+                                    int S) {
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < S; s += gridDim.x * blockDim.x)
+    if (fallback[s] != 0) pool_next[s] += 1;
+}
+}  // namespace
+
+cudaError_t launch_pool_advance(const Dims& dm, const uint8_t* fallback, int32_t* pool_next,
+                                cudaStream_t stream) {
+  if (dm.S <= 0) return cudaSuccess;
+  pool_advance_kernel<<<(dm.S + 255) / 256, 256, 0, stream>>>(fallback, pool_next, dm.S);
   return cudaGetLastError();
 }
 

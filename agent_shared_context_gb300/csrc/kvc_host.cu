@@ -102,6 +102,11 @@ kvc_status check_params(const kvc_segments* seg, const kvc_params* prm, bool nee
   }
   if (need_rank) {
     if (!(prm->tau >= 0.0f)) return fail(KVC_ERR_INVALID_ARGUMENT, "tau must be >= 0 (not NaN)");
+    if (prm->select_mode != 0 && prm->select_mode != 1)
+      return fail(KVC_ERR_INVALID_ARGUMENT, "select_mode = %d is neither 0 nor 1",
+                  prm->select_mode);
+    if (prm->select_mode == 1 && !(prm->reuse_ratio >= 0.0f && prm->reuse_ratio <= 1.0f))
+      return fail(KVC_ERR_INVALID_ARGUMENT, "reuse_ratio must lie in [0, 1]");
   }
   if (need_build) {
     const int l = r + prm->oversample;
@@ -329,6 +334,55 @@ kvc_status kvc_build_states(const kvc_segments* seg, const kvc_params* prm,
   return KVC_OK;
 }
 
+// --------------------------------------------------------------- pool
+kvc_status kvc_pool_insert(const kvc_segments* seg, const kvc_params* prm, kvc_cache_view dense_K,
+                           kvc_cache_view dense_V, kvc_cache_view held_K, kvc_cache_view held_V,
+                           const float* omega, const uint8_t* fallback, int32_t* pool_next,
+                           void* U_K, void* W_K, void* U_V, void* W_V, float* summaries,
+                           float* sigma, int32_t* eff_rank, void* workspace,
+                           size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
+  static thread_local SegTable tab;
+  KVC_TRY(check_segments(seg, &tab));
+  KVC_TRY(check_params(seg, prm, false, false, true));
+  KVC_TRY(check_view(seg, dense_K, "dense_K"));
+  KVC_TRY(check_view(seg, dense_V, "dense_V"));
+  KVC_TRY(check_view(seg, held_K, "held_K"));
+  KVC_TRY(check_view(seg, held_V, "held_V"));
+  KVC_TRY(check_dev_ptr(omega, "omega"));
+  KVC_TRY(check_dev_ptr(fallback, "fallback"));
+  KVC_TRY(check_dev_ptr(pool_next, "pool_next"));
+  KVC_TRY(check_dev_ptr(U_K, "U_K", true));
+  KVC_TRY(check_dev_ptr(W_K, "W_K", true));
+  KVC_TRY(check_dev_ptr(U_V, "U_V", true));
+  KVC_TRY(check_dev_ptr(W_V, "W_V", true));
+  KVC_TRY(check_dev_ptr(summaries, "summaries"));
+  KVC_TRY(check_dev_ptr(sigma, "sigma"));
+  KVC_TRY(check_dev_ptr(eff_rank, "eff_rank"));
+  KVC_TRY(check_dev_ptr(dev_status, "dev_status"));
+  const Dims dm = make_dims(seg, prm);
+  const int l = prm->rank + prm->oversample;
+  const size_t need = build_workspace_bytes(dm, l);
+  if (need > 0) {
+    if (workspace == nullptr || workspace_bytes < need)
+      return fail(KVC_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need,
+                  workspace_bytes);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return fail(KVC_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  }
+  if (seg->S == 0) return KVC_OK;
+  const View ex[2] = {to_view(dense_K), to_view(dense_V)};
+  const View rf[2] = {to_view(held_K), to_view(held_V)};
+  void* Us[2] = {U_K, U_V};
+  void* Ws[2] = {W_K, W_V};
+  cudaError_t e = launch_build(dm, tab, seg->dtype, ex, rf, omega, l, prm->power_iters,
+                               prm->energy_frac, 0, Us, Ws, sigma, eff_rank, workspace,
+                               dev_status, stream, fallback, pool_next, summaries);
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_pool_insert build launch");
+  e = launch_pool_advance(dm, fallback, pool_next, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_pool_insert cursor launch");
+  return KVC_OK;
+}
+
 // --------------------------------------------------------------- match
 kvc_status kvc_match_anchors(const kvc_segments* seg, const kvc_params* prm, kvc_cache_view ref_K,
                              const float* summaries, float* weights, int32_t* best, float* query,
@@ -369,6 +423,12 @@ static kvc_status apply_impl(const kvc_segments* seg, const kvc_params* prm, con
   if (e != cudaSuccess) return cuda_fail(e, "correction apply launch");
   e = launch_segment_reduce(dm, partial, prm->tau, score, fallback, stream);
   if (e != cudaSuccess) return cuda_fail(e, "segment reduce launch");
+  if (prm->select_mode == 1) {
+    const int n_reuse = static_cast<int>(
+        std::floor(static_cast<double>(prm->reuse_ratio) * seg->S + 0.5));
+    e = launch_select_ratio(dm, score, std::min(std::max(n_reuse, 0), seg->S), fallback, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reuse-ratio select launch");
+  }
   return KVC_OK;
 }
 

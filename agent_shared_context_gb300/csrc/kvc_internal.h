@@ -77,6 +77,10 @@ cudaError_t launch_apply_simt(const Dims& dm, const SegTable& seg, const View re
 cudaError_t launch_segment_reduce(const Dims& dm, const float* partial, float tau, float* score,
                                   uint8_t* fallback, cudaStream_t stream);
 
+// Reuse-ratio mode: flag the S - n_reuse segments with the largest scores.
+cudaError_t launch_select_ratio(const Dims& dm, const float* score, int n_reuse,
+                                uint8_t* fallback, cudaStream_t stream);
+
 // Bit-exact copy of the dense rows of every flagged segment into out.
 cudaError_t launch_fallback_copy(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
                                  const View densev[2], const View outv[2],
@@ -88,7 +92,12 @@ cudaError_t launch_build(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
                          const View exactv[2], const View refv[2], const float* omega, int l,
                          int q, float energy_frac, int slot, void* U[2], void* W[2],
                          float* sigma, int32_t* eff_rank, void* workspace, int32_t* dev_status,
-                         cudaStream_t stream);
+                         cudaStream_t stream, const uint8_t* seg_mask = nullptr,
+                         const int32_t* seg_slot = nullptr, float* summaries = nullptr);
+
+// Anchor pool: pool_next[s] += 1 for every flagged segment.
+cudaError_t launch_pool_advance(const Dims& dm, const uint8_t* fallback, int32_t* pool_next,
+                                cudaStream_t stream);
 
 // Bounded-wait self test.
 cudaError_t launch_selftest_wait(int32_t max_polls, int32_t* dev_status, cudaStream_t stream);

@@ -44,7 +44,7 @@ KVC_F32 = 1
 EXPORTS = ("kvc_version", "kvc_status_string", "kvc_last_error",
            "kvc_build_states_workspace", "kvc_build_states", "kvc_match_anchors",
            "kvc_apply_correction", "kvc_chain_edge_workspace", "kvc_chain_edge",
-           "kvc_selftest_bounded_wait", "kvc_chain_edge_noalloc")
+           "kvc_selftest_bounded_wait", "kvc_chain_edge_noalloc", "kvc_pool_insert")
 
 KVC_NOALLOC_MAX_UNITS = 262144
 
@@ -76,7 +76,8 @@ class kvc_params(ctypes.Structure):
     _fields_ = [("rank", ctypes.c_int32), ("oversample", ctypes.c_int32),
                 ("power_iters", ctypes.c_int32), ("n_anchors", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("energy_frac", ctypes.c_float),
-                ("temperature", ctypes.c_float), ("tau", ctypes.c_float)]
+                ("temperature", ctypes.c_float), ("tau", ctypes.c_float),
+                ("select_mode", ctypes.c_int32), ("reuse_ratio", ctypes.c_float)]
 
 
 _VIEW = kvc_cache_view
@@ -94,6 +95,9 @@ lib.kvc_build_states_workspace.argtypes = [_SEG_P, _PRM_P]
 lib.kvc_build_states.restype = _ST
 lib.kvc_build_states.argtypes = [_SEG_P, _PRM_P, _VIEW, _VIEW, _VIEW, _VIEW, _VP, ctypes.c_int32,
                                  _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP, _VP]
+lib.kvc_pool_insert.restype = _ST
+lib.kvc_pool_insert.argtypes = [_SEG_P, _PRM_P, _VIEW, _VIEW, _VIEW, _VIEW, _VP, _VP, _VP, _VP, _VP,
+                                _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP, _VP]
 lib.kvc_match_anchors.restype = _ST
 lib.kvc_match_anchors.argtypes = [_SEG_P, _PRM_P, _VIEW, _VP, _VP, _VP, _VP, _VP, _VP]
 lib.kvc_apply_correction.restype = _ST
@@ -183,9 +187,12 @@ class Segments:
 
 def params(rank: int = 32, oversample: int = 8, power_iters: int = 2, n_anchors: int = 8,
            top_k: int = 0, energy_frac: float = 0.9, temperature: float = 0.1,
-           tau: float = 0.32) -> kvc_params:
+           tau: float = 0.32, reuse_ratio: Optional[float] = None) -> kvc_params:
+    """Method parameters; ``reuse_ratio`` switches to the reuse-ratio mode."""
     return kvc_params(rank, oversample, power_iters, n_anchors,
-                      top_k if top_k > 0 else n_anchors, energy_frac, temperature, tau)
+                      top_k if top_k > 0 else n_anchors, energy_frac, temperature, tau,
+                      0 if reuse_ratio is None else 1,
+                      0.0 if reuse_ratio is None else float(reuse_ratio))
 
 
 def params_from_workload(wl, **over) -> kvc_params:
@@ -230,6 +237,20 @@ def kvc_build_states(seg: Segments, prm: kvc_params, exact_K, exact_V, ref_K, re
                               _addr(U_V), _addr(W_V), _addr(sigma), _addr(eff_rank),
                               _addr(workspace), ws_bytes, _addr(dev_status), _stream(stream))
     return _done(st, "kvc_build_states", check)
+
+
+def kvc_pool_insert(seg: Segments, prm: kvc_params, dense_K, dense_V, held_K, held_V,
+                    omega: Ptr, fallback: Ptr, pool_next: Ptr, U_K: Ptr, W_K: Ptr, U_V: Ptr,
+                    W_V: Ptr, summaries: Ptr, sigma: Ptr, eff_rank: Ptr, workspace: Ptr,
+                    dev_status: Ptr, stream=None, workspace_bytes: Optional[int] = None,
+                    check: bool = True) -> int:
+    ws_bytes = _nbytes(workspace) if workspace_bytes is None else int(workspace_bytes)
+    st = lib.kvc_pool_insert(seg.ref, ctypes.byref(prm), _v(dense_K), _v(dense_V), _v(held_K),
+                             _v(held_V), _addr(omega), _addr(fallback), _addr(pool_next),
+                             _addr(U_K), _addr(W_K), _addr(U_V), _addr(W_V), _addr(summaries),
+                             _addr(sigma), _addr(eff_rank), _addr(workspace), ws_bytes,
+                             _addr(dev_status), _stream(stream))
+    return _done(st, "kvc_pool_insert", check)
 
 
 def kvc_match_anchors(seg: Segments, prm: kvc_params, ref_K, summaries: Ptr, weights: Ptr,

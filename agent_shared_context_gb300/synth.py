@@ -240,7 +240,13 @@ def _haar(batch: int, n: int, m: int, g: torch.Generator, device) -> torch.Tenso
     (Mezzadri, "How to generate random matrices from the classical compact
     groups", Notices AMS 2007)."""
     G = _randn((batch, n, m), g, device)
-    Q, Rm = torch.linalg.qr(G, mode="reduced")
+    try:
+        Q, Rm = torch.linalg.qr(G, mode="reduced")
+    except RuntimeError:
+        # Some tool environments (e.g. under a profiler) cannot load the
+        # CUDA linear-algebra backend; factor the same Gaussian on the host.
+        Qc, Rc = torch.linalg.qr(G.cpu(), mode="reduced")
+        Q, Rm = Qc.to(G.device), Rc.to(G.device)
     sgn = torch.sign(torch.diagonal(Rm, dim1=-2, dim2=-1))
     sgn = torch.where(sgn == 0, torch.ones_like(sgn), sgn)
     return Q * sgn.unsqueeze(-2)

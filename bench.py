@@ -41,10 +41,12 @@ KERNEL_SRC = os.path.join(ROOT, "agent_shared_context_gb300", "csrc", "kvc_apply
 def _args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
     p.add_argument("--workload", default="llama2k")
+    p.add_argument("--requests", type=int, default=0,
+                   help="use only the first N requests of the workload (small profiling cases)")
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -111,7 +113,7 @@ class ClockSampler:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -299,6 +301,31 @@ def run_kvc(args, wl):
     achieved = apply_bytes / (apply_ms / 1000.0) / 1e9
     traffic = _profile_traffic(wl.name)
 
+    # ---- state builder (workloads that build anchor states), timed alone
+    builder = None
+    if runner.build:
+        eo1 = runner.edges[1]
+        evb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(3)]
+        for i in range(4):
+            if i >= 1:
+                evb[i - 1][0].record(stream)
+            kvc.kvc_build_states(seg, prm, inp.exact_K[1], inp.exact_V[1], inp.exact_K[0],
+                                 inp.exact_V[0], inp.omega, wl.build_slot, e.U_K, e.W_K, e.U_V,
+                                 e.W_V, eo1.sigma, eo1.eff_rank, runner.build_ws,
+                                 runner.dev_status)
+            if i >= 1:
+                evb[i - 1][1].record(stream)
+        torch.cuda.synchronize(dev)
+        b_ms = statistics.mean(a.elapsed_time(b) for a, b in evb)
+        mats = wl.S * wl.L * wl.H * 2
+        gemm_flop = 0
+        for s in range(wl.S):
+            gemm_flop += wl.L * wl.H * 2 * 2 * (2 * wl.power_iters + 2) * wl.seg_len[s] * wl.d * wl.l
+        builder = {"kernel": "build_simt_kernel", "launch_ms": b_ms, "matrices": mats,
+                   "gemm_tflops": gemm_flop / (b_ms / 1000.0) / 1e12,
+                   "tensor_pipe": "not used (FP32 FMA builder)"}
+
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e and world == 1:
@@ -321,6 +348,7 @@ def run_kvc(args, wl):
                      "algorithmic_bytes_per_launch": apply_bytes, "launch_ms": apply_ms},
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
+        "builder": builder,
         "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -387,6 +415,14 @@ def main():
     args = _args()
     from agent_shared_context_gb300 import synth
     wl = synth.workload(args.workload)
+    if 0 < args.requests < wl.R:
+        import dataclasses
+        keep = [s for s in range(wl.S) if wl.seg_request[s] < args.requests]
+        wl = dataclasses.replace(
+            wl, R=args.requests, name="%s-r%d" % (wl.name, args.requests),
+            seg_request=tuple(wl.seg_request[s] for s in keep),
+            seg_start=tuple(wl.seg_start[s] for s in keep),
+            seg_len=tuple(wl.seg_len[s] for s in keep))
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -142,6 +142,11 @@ typedef struct kvc_params {
   float energy_frac;    /* effective-rank fraction, (0, 1]; pages: 0.9        */
   float temperature;    /* softmax temperature > 0                            */
   float tau;            /* reliability threshold >= 0 (listing, Table 3)      */
+  int32_t select_mode;  /* 0: fallback iff score > tau (listing, Figure 1(a));  */
+                        /* 1: reuse-ratio mode: round(reuse_ratio * S) segments */
+                        /*    are reused, the rest -- largest scores, ties to   */
+                        /*    the lower index -- fall back (listing, Figure 5)  */
+  float reuse_ratio;    /* rho in [0, 1], read when select_mode == 1          */
 } kvc_params;
 
 /* Library version string, e.g. "0.1.0 sm_103a". */
@@ -175,6 +180,29 @@ kvc_status kvc_build_states(const kvc_segments* seg, const kvc_params* prm,
                             float* sigma, int32_t* eff_rank,
                             void* workspace, size_t workspace_bytes,
                             int32_t* dev_status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * kvc_pool_insert -- online anchor-pool maintenance (listing, Figure 1(b):
+ * online anchors per shared segment; Table 13: pool capacity V).
+ *
+ * For every segment s with fallback[s] != 0 (device flags, e.g. from
+ * kvc_chain_edge): slot = pool_next[s] mod n_anchors (FIFO eviction); the
+ * state of (dense - held) over the segment's rows is built into that slot
+ * exactly as kvc_build_states does (U rows >= len zeroed), the slot's
+ * summary becomes the mean of held_K over the segment, sigma / eff_rank of
+ * the segment are written, and pool_next[s] is incremented.  Unflagged
+ * segments, other slots and their sigma / eff_rank entries are untouched.
+ * pool_next is a caller-owned device int32 [S] cursor.  Same workspace as
+ * kvc_build_states.
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_pool_insert(const kvc_segments* seg, const kvc_params* prm,
+                           kvc_cache_view dense_K, kvc_cache_view dense_V,
+                           kvc_cache_view held_K, kvc_cache_view held_V,
+                           const float* omega, const uint8_t* fallback, int32_t* pool_next,
+                           void* U_K, void* W_K, void* U_V, void* W_V, float* summaries,
+                           float* sigma, int32_t* eff_rank,
+                           void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * kvc_match_anchors -- match the current cache to the segment's anchors and

@@ -44,10 +44,14 @@ R7  reliability score of a segment = sqrt(sum |C|^2 / sum |ref|^2) over all
     reference gives 0 if the correction is also zero, else +inf.
 R8  fallback granularity = one PH segment; a fallback segment takes the dense
     (exact) rows.  Edge 0 (agent A0) is exact and passes through.
+R11 anchor-pool insertion: a fallback segment's (dense - held) state goes
+    into slot pool_next mod A (FIFO), its summary is the held key mean.
 R9  randomized state: Y = delta Omega, HMT Algorithm 4.4 with q power
     iterations and Householder QR, B = Q^T delta, SVD of B, keep r.  The
     effective rank of the state uses the l singular values of B against
     |delta|_F^2 and returns l + 1 when they retain less than the fraction.
+R10 reuse-ratio mode: round(rho * S) segments are reused, the others (the
+    largest scores, ties by lower index first) fall back.
 
 Every function below is pinned by ``tests/test_oracle_pins.py`` against
 closed forms, special cases reducing to textbook routines, invariants, or
@@ -63,7 +67,8 @@ import numpy as np
 __all__ = [
     "eff_rank", "exact_state", "randomized_state", "build_unit", "build_states",
     "query_summary", "cosine", "select_and_weight", "match_anchors",
-    "apply_correction", "segment_scores", "chain_edge", "chain",
+    "apply_correction", "segment_scores", "select_by_reuse_ratio", "pool_insert",
+    "chain_edge", "chain",
     "relative_error", "Segments", "States",
 ]
 
@@ -334,6 +339,24 @@ def segment_scores(partial: np.ndarray, tau: float):
     return score, fallback
 
 
+def select_by_reuse_ratio(score: Sequence[float], rho: float) -> np.ndarray:
+    """Reuse-ratio-targeted fallback (reading R10).
+
+    The efficiency experiments of the listing fix the reuse ratio rho
+    directly (Figure 5, Tables 11-12: rho = 0.95 ... 0.6) instead of a
+    threshold.  Reading: of the S segments of a batch, round(rho * S) (half
+    up) are reused and the rest -- those with the largest scores, ordered by
+    (-score, index) -- fall back.  Returns fallback [S] bool."""
+    S = len(score)
+    n_reuse = int(math.floor(rho * S + 0.5))
+    n_reuse = max(0, min(S, n_reuse))
+    order = sorted(range(S), key=lambda s: (-float(score[s]), s))
+    fallback = np.zeros(S, dtype=bool)
+    for s in order[:S - n_reuse]:
+        fallback[s] = True
+    return fallback
+
+
 # ---------------------------------------------------------------------------
 # O8  one edge and the chain (Figure 1(c), Figure 3, KVCMAS abstract)
 # ---------------------------------------------------------------------------
@@ -341,7 +364,7 @@ def chain_edge(edge: int, ref: Tuple[np.ndarray, np.ndarray], seg: Segments,
                summaries: np.ndarray, states: States, top_k: int,
                temperature: float, tau: float,
                dense: Optional[Tuple[np.ndarray, np.ndarray]],
-               out_init: Tuple[np.ndarray, np.ndarray]):
+               out_init: Tuple[np.ndarray, np.ndarray], reuse_ratio: Optional[float] = None):
     """One workflow edge.  Edge 0 returns ``ref`` unchanged (A0 is exact).
 
     For edge >= 1: match (O3-O5), correct (O6), score (O7); every flagged
@@ -352,6 +375,8 @@ def chain_edge(edge: int, ref: Tuple[np.ndarray, np.ndarray], seg: Segments,
     weights, best, query = match_anchors(ref[0], seg, summaries, top_k, temperature)
     cK, cV, partial = apply_correction(ref, seg, states, weights)
     score, fallback = segment_scores(partial, tau)
+    if reuse_ratio is not None:
+        fallback = select_by_reuse_ratio(score, reuse_ratio)
     out = [np.array(out_init[0], np.float64, copy=True), np.array(out_init[1], np.float64, copy=True)]
     for s in range(seg.S):
         req, t0, n = seg.request[s], seg.start[s], seg.length[s]
@@ -367,7 +392,7 @@ def chain_edge(edge: int, ref: Tuple[np.ndarray, np.ndarray], seg: Segments,
 def chain(exact_K: List[np.ndarray], exact_V: List[np.ndarray], seg: Segments,
           edge_states: List[States], edge_summaries: List[np.ndarray], top_k: int,
           temperature: float, tau: float, use_dense: bool = True,
-          build: Optional[dict] = None):
+          build: Optional[dict] = None, reuse_ratio: Optional[float] = None):
     """Run agents A0 -> A1 -> ... along the chain.
 
     held_0 = exact_0; for edge j >= 1 the reference is held_{j-1}.  When
@@ -388,11 +413,54 @@ def chain(exact_K: List[np.ndarray], exact_V: List[np.ndarray], seg: Segments,
             extra = dict(sigma=sigma, eff_rank=erank, states=states)
         dense = (exact_K[j], exact_V[j]) if use_dense else None
         res = chain_edge(j, held, seg, edge_summaries[j - 1], states, top_k, temperature,
-                         tau, dense, (exact_K[j], exact_V[j]))
+                         tau, dense, (exact_K[j], exact_V[j]), reuse_ratio)
         res.update(extra)
         results.append(res)
         held = (res["out_K"], res["out_V"])
     return results
+
+
+def pool_insert(dense: Tuple[np.ndarray, np.ndarray], held: Tuple[np.ndarray, np.ndarray],
+                seg: Segments, fallback: Sequence[bool], pool_next: np.ndarray,
+                states: States, summaries: np.ndarray, r: int, omega: np.ndarray, q: int,
+                frac: float = 0.9):
+    """Online anchor-pool maintenance (reading R11).
+
+    The listing keeps V online anchors per shared segment (Table 13: V = 1,
+    5, 10, 20) and, for a segment that falls back to dense prefill, the
+    dense result is exactly what a new anchor needs: its delta against the
+    held cache.  For every flagged segment s: slot = pool_next[s] mod A (FIFO
+    eviction); build the state of (dense - held) into that slot (O2); the
+    slot's summary becomes the mean of the held keys over the segment (the
+    representation later caches are matched against, O3); pool_next[s] += 1.
+    Unflagged segments are untouched.  Updates states, summaries and
+    pool_next in place; returns (sigma, eff_rank) of the inserted states
+    (zeros for other segments)."""
+    L, H = held[0].shape[1], held[0].shape[2]
+    A = summaries.shape[3]
+    l = omega.shape[1]
+    sigma = np.zeros((seg.S, L, H, 2, l))
+    erank = np.zeros((seg.S, L, H, 2), dtype=np.int64)
+    for s in range(seg.S):
+        if not fallback[s]:
+            continue
+        slot = int(pool_next[s]) % A
+        req, t0, n = seg.request[s], seg.start[s], seg.length[s]
+        for layer in range(L):
+            for head in range(H):
+                for kv in range(2):
+                    U, W, sv, er = build_unit(dense[kv][req, layer, head, t0:t0 + n, :],
+                                              held[kv][req, layer, head, t0:t0 + n, :],
+                                              r, omega, q, frac)
+                    states.U[kv][s, layer, head, :, slot, :] = 0.0
+                    states.U[kv][s, layer, head, :n, slot, :] = U
+                    states.W[kv][s, layer, head, :, slot, :] = W
+                    sigma[s, layer, head, kv, :] = sv
+                    erank[s, layer, head, kv] = er
+                summaries[s, layer, head, slot, :] = query_summary(
+                    held[0][req, layer, head, t0:t0 + n, :])
+        pool_next[s] += 1
+    return sigma, erank
 
 
 def relative_error(approx: np.ndarray, target: np.ndarray) -> float:

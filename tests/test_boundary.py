@@ -234,3 +234,13 @@ def test_binding_raises_with_message():
                                  a.dev_status, stream=0)
     assert ei.value.status == kvc.KVC_ERR_INVALID_ARGUMENT
     assert "U_K" in str(ei.value)
+
+
+def test_reuse_ratio_mode_validation():
+    a = Args()
+    assert a.apply(prm=kvc.params(rank=32, n_anchors=8, top_k=8, reuse_ratio=1.5)) == kvc.KVC_ERR_INVALID_ARGUMENT
+    assert a.apply(prm=kvc.params(rank=32, n_anchors=8, top_k=8, reuse_ratio=-0.1)) == kvc.KVC_ERR_INVALID_ARGUMENT
+    p = kvc.params(rank=32, n_anchors=8, top_k=8)
+    p.select_mode = 2
+    assert a.apply(prm=p) == kvc.KVC_ERR_INVALID_ARGUMENT
+    assert "select_mode" in kvc.lib.kvc_last_error().decode()

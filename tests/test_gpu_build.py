@@ -184,3 +184,63 @@ def test_chain_with_builder_matches_oracle(name):
         er_o = res[j]["eff_rank"]
         agree = float(np.mean(er_g == er_o))
         assert agree >= 0.9, (j, er_g, er_o)
+
+
+@pytest.mark.parametrize("name", ["tiny-f32", "longctx-small"])
+def test_pool_insert_matches_oracle(name):
+    """kvc_pool_insert against O.pool_insert: only flagged segments gain an
+    anchor, in slot pool_next mod A (FIFO); the slot's state is the built
+    (dense - held) state, its summary the held key mean; cursors advance."""
+    kvc = _kvc()
+    wl = _cases()[name]
+    wl = dataclasses.replace(wl, A=max(wl.A, 3))
+    inp = synth.generate(wl, device="cuda", edges=[1])
+    e = inp.edges[0]
+    seg = kvc.Segments.from_workload(wl)
+    prm = kvc.params_from_workload(wl)
+    S, L, H, l, A = wl.S, wl.L, wl.H, wl.l, wl.A
+    flags = [1 if s % 2 == 0 else 0 for s in range(S)]
+    fb = torch.tensor(flags, dtype=torch.uint8, device="cuda")
+    cursor0 = [5 + 2 * s for s in range(S)]
+    cur = torch.tensor(cursor0, dtype=torch.int32, device="cuda")
+    U_K, W_K, U_V, W_V = (x.clone() for x in (e.U_K, e.W_K, e.U_V, e.W_V))
+    summ = e.summaries.clone()
+    sigma = torch.zeros((S, L, H, 2, l), device="cuda")
+    erank = torch.zeros((S, L, H, 2), dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(kvc.kvc_build_states_workspace(seg, prm), 256), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvc.kvc_pool_insert(seg, prm, inp.exact_K[1], inp.exact_V[1], inp.exact_K[0], inp.exact_V[0],
+                        inp.omega, fb, cur, U_K, W_K, U_V, W_V, summ, sigma, erank, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ost = O.States(np64(e.U_K), np64(e.W_K), np64(e.U_V), np64(e.W_V))
+    osumm = np64(e.summaries)
+    ocur = np.array(cursor0)
+    seg_o = O.Segments(wl.seg_request, wl.seg_start, wl.seg_len)
+    osig, oer = O.pool_insert((np64(inp.exact_K[1]), np64(inp.exact_V[1])),
+                              (np64(inp.exact_K[0]), np64(inp.exact_V[0])), seg_o,
+                              [bool(f) for f in flags], ocur, ost, osumm, wl.r, np64(inp.omega),
+                              wl.power_iters, wl.energy_frac)
+    assert cur.cpu().numpy().tolist() == ocur.tolist()
+    tol = 1e-4 if wl.dtype == "f32" else 2e-2
+    for s in range(S):
+        for kv, (Ug, Wg) in enumerate(((U_K, W_K), (U_V, W_V))):
+            orig_U = (e.U_K, e.U_V)[kv]
+            if not flags[s]:
+                assert torch.equal(Ug[s], orig_U[s])
+                continue
+            slot = cursor0[s] % A
+            for a in range(A):
+                if a != slot:
+                    assert torch.equal(Ug[s, :, :, :, a], orig_U[s, :, :, :, a])
+            n = wl.seg_len[s]
+            for layer in range(L):
+                for h in range(H):
+                    pg = np64(Ug[s, layer, h, :n, slot]) @ np64(Wg[s, layer, h, :, slot]).T
+                    po = ost.U[kv][s, layer, h, :n, slot] @ ost.W[kv][s, layer, h, :, slot].T
+                    assert O.relative_error(pg, po) <= tol
+        if flags[s]:
+            np.testing.assert_allclose(np64(summ[s]), osumm[s], rtol=0, atol=1e-5)
+        else:
+            assert torch.equal(summ[s], e.summaries[s])

@@ -1,0 +1,144 @@
+"""Parity at the workloads' full sizes, in the launch configuration the bench
+times (the whole batch in one kvc_chain_edge call per edge).
+
+The GPU runs the complete workload; the oracle recomputes a sample of
+segments from the same generator tensors.  Segments are independent (their
+own rows, states, score and flag), so the oracle's chain over the sampled
+segments alone is exactly the full computation restricted to them.
+Tolerances are those of tests/test_gpu_parity.py.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from agent_shared_context_gb300 import synth
+from agent_shared_context_gb300.synth import EdgeInputs, WorkloadInputs
+
+from ._harness import check_out, np64, oracle_chain, sim_gaps
+
+pytestmark = pytest.mark.gpu
+
+
+def restrict(wl, inp, q, segs):
+    """Sub-workload holding request q only and the listed segments of it."""
+    sub = dataclasses.replace(
+        wl, R=1, name=wl.name + "-sample",
+        seg_request=tuple(0 for _ in segs),
+        seg_start=tuple(wl.seg_start[s] for s in segs),
+        seg_len=tuple(wl.seg_len[s] for s in segs))
+    idx = torch.tensor(segs, device=inp.exact_K[0].device)
+    Tm = sub.max_seg_len
+    edges = []
+    for e in inp.edges:
+        if e is None:
+            edges.append(None)
+            continue
+        edges.append(EdgeInputs(
+            U_K=e.U_K.index_select(0, idx)[:, :, :, :Tm].contiguous(),
+            W_K=e.W_K.index_select(0, idx),
+            U_V=e.U_V.index_select(0, idx)[:, :, :, :Tm].contiguous(),
+            W_V=e.W_V.index_select(0, idx),
+            summaries=e.summaries.index_select(0, idx),
+            planted=e.planted[segs]))
+    return sub, WorkloadInputs(wl=sub, exact_K=[E[q:q + 1] for E in inp.exact_K],
+                               exact_V=[E[q:q + 1] for E in inp.exact_V], edges=edges,
+                               omega=inp.omega, planted_ratio=inp.planted_ratio)
+
+
+def _compare(wl, runner, sub, sub_inp, q, segs, build):
+    res, (_, _, _, _, summ) = oracle_chain(sub, sub_inp, build=build)
+    for j in range(1, wl.edges + 1):
+        eo = runner.edges[j]
+        fb_g = eo.fallback.cpu().numpy().astype(bool)[segs]
+        assert np.array_equal(fb_g, res[j]["fallback"]), (j, fb_g, res[j]["score"])
+        sc_g = eo.score.cpu().numpy()[segs]
+        np.testing.assert_allclose(sc_g, res[j]["score"], rtol=2e-3 if j == 1 else 1e-2)
+        w_g = eo.weights.cpu().numpy()[segs]
+        if j == 1 and not build:
+            np.testing.assert_allclose(w_g, res[j]["weights"], rtol=0, atol=2e-4)
+            gap = 1e-5
+        else:
+            np.testing.assert_allclose(w_g, res[j]["weights"], rtol=1e-2 if not build else 5e-2,
+                                       atol=1e-4 if not build else 1e-3)
+            gap = 2e-3
+        sure = sim_gaps(res[j]["query"], summ[j - 1]) >= gap
+        assert np.array_equal(eo.best.cpu().numpy()[segs][sure], res[j]["best"][sure])
+        for key in ("out_K", "out_V"):
+            out_g = np64(getattr(eo, key)[q:q + 1])
+            if not build:
+                check_out(sub, j, out_g, res[j][key], res[j - 1][key], res[j]["fallback"], True)
+                continue
+            # the built slot adds the builder tolerance (2e-2 of U W^T) to C
+            for s in range(sub.S):
+                if res[j]["fallback"][s]:
+                    continue
+                t0, n = sub.seg_start[s], sub.seg_len[s]
+                g = out_g[0, :, :, t0:t0 + n]
+                o = res[j][key][0, :, :, t0:t0 + n]
+                r = res[j - 1][key][0, :, :, t0:t0 + n]
+                for layer in range(sub.L):
+                    for h in range(sub.H):
+                        err = np.linalg.norm(g[layer, h] - o[layer, h])
+                        c = np.linalg.norm(o[layer, h] - r[layer, h])
+                        assert err <= 2e-2 * c + j * 2.0 ** -8 * np.linalg.norm(o[layer, h])
+
+
+def _run(wl, build=False):
+    from agent_shared_context_gb300.chain import ChainRunner
+    inp = synth.generate(wl, device="cuda")
+    originals = inp.edges
+    if build:   # the runner overwrites the built slot; keep the generator's states
+        originals = [None if e is None else dataclasses.replace(
+            e, U_K=e.U_K.clone(), W_K=e.W_K.clone(), U_V=e.U_V.clone(), W_V=e.W_V.clone())
+            for e in inp.edges]
+    runner = ChainRunner(wl, inp, device="cuda", build=build)
+    runner.run()
+    torch.cuda.synchronize()
+    assert int(runner.dev_status.item()) == 0
+    return dataclasses.replace(inp, edges=originals), runner
+
+
+def test_llama2k_full_size_sampled_requests():
+    wl = synth.workload("llama2k")
+    inp, runner = _run(wl)
+    planted = inp.edges[0].planted
+    q_pl = int(torch.nonzero(planted)[0]) if bool(planted.any()) else 0
+    for q in sorted({q_pl, 0}):
+        segs = [s for s in range(wl.S) if wl.seg_request[s] == q]
+        sub, sub_inp = restrict(wl, inp, q, segs)
+        _compare(wl, runner, sub, sub_inp, q, segs, build=False)
+
+
+def test_concurrent_full_size_first_edge_sampled_segments():
+    wl = dataclasses.replace(synth.workload("concurrent"), n_agents=2)
+    inp, runner = _run(wl)
+    q = 0
+    segs = [s for s in range(wl.S) if wl.seg_request[s] == q][:3]
+    sub, sub_inp = restrict(wl, inp, q, segs)
+    _compare(wl, runner, sub, sub_inp, q, segs, build=False)
+    # PF rows of every request are untouched by the whole-batch call
+    eo = runner.edges[1]
+    mask = torch.ones((wl.R, wl.T), dtype=torch.bool)
+    for s in range(wl.S):
+        mask[wl.seg_request[s], wl.seg_start[s]:wl.seg_start[s] + wl.seg_len[s]] = False
+    for r in range(wl.R):
+        pf = mask[r].cuda()
+        assert torch.equal(eo.out_K[r][:, :, pf, :], inp.exact_K[1][r][:, :, pf, :])
+
+
+def test_vl_full_size_sampled_segments_with_tail():
+    wl = synth.workload("vl")
+    inp, runner = _run(wl)
+    segs = [2, 5, 17]                   # visual-block segments and the 296-token tail
+    sub, sub_inp = restrict(wl, inp, 0, segs)
+    _compare(wl, runner, sub, sub_inp, 0, segs, build=False)
+
+
+def test_longctx_full_size_with_builder_sampled_segments():
+    wl = synth.workload("longctx")
+    inp, runner = _run(wl, build=True)
+    segs = [0, 37]
+    sub, sub_inp = restrict(wl, inp, 0, segs)
+    _compare(wl, runner, sub, sub_inp, 0, segs, build=True)

@@ -302,3 +302,44 @@ def test_device_timeout_reports_status():
     assert int(st.item()) == kvc.KVC_ERR_DEVICE_TIMEOUT
     x = torch.ones(16, device="cuda") * 2
     assert float(x.sum()) == 32.0
+
+
+def test_reuse_ratio_mode_on_gpu():
+    """Reuse-ratio mode (listing, Figure 5): exactly S - round(rho*S) segments
+    fall back, they hold the largest scores, and the set matches the oracle's
+    selection wherever the oracle's boundary scores are >= 1e-3 apart."""
+    kvc = _kvc()
+    wl = synth.scaled(synth.workload("concurrent"), L=2, H=2, R=3, seg_len=[130, 100, 77], pf=8,
+                      fallback_frac=0.0)
+    inp = _edge1_setup(wl)
+    seg_o, EK, EV, states, summ = oracle_inputs(wl, inp)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    w = torch.rand((wl.S, wl.L, wl.H, wl.A), generator=g, device="cuda")
+    _, _, opart = O.apply_correction((EK[0], EV[0]), seg_o, states[0], np64(w))
+    osc, _ = O.segment_scores(opart, wl.tau)
+    e = inp.edges[0]
+    seg = kvc.Segments.from_workload(wl)
+    for rho in (0.0, 0.34, 0.5, 0.67, 0.9, 1.0):
+        prm = kvc.params_from_workload(wl, reuse_ratio=rho)
+        oK = torch.empty_like(inp.exact_K[0])
+        oV = torch.empty_like(inp.exact_V[0])
+        part = torch.empty((wl.S, wl.L, wl.H, 4), device="cuda")
+        score = torch.empty((wl.S,), device="cuda")
+        fb = torch.empty((wl.S,), dtype=torch.uint8, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kvc.kvc_apply_correction(seg, prm, inp.exact_K[0], inp.exact_V[0], e.U_K, e.W_K, e.U_V,
+                                 e.W_V, w, oK, oV, part, score, fb, st)
+        torch.cuda.synchronize()
+        fbg = fb.cpu().numpy().astype(bool)
+        scg = score.cpu().numpy()
+        n_reuse = int(math.floor(np.float32(rho) * wl.S + 0.5))
+        assert fbg.sum() == wl.S - n_reuse
+        if fbg.any() and (~fbg).any():
+            assert scg[fbg].min() >= scg[~fbg].max()
+        ofb = O.select_by_reuse_ratio(osc, float(np.float32(rho)))
+        srt = np.sort(osc)[::-1]
+        k = wl.S - n_reuse
+        if 0 < k < wl.S and (srt[k - 1] - srt[k]) < 1e-3 * srt[k - 1]:
+            continue
+        assert np.array_equal(fbg, ofb), (rho, fbg, ofb, osc)

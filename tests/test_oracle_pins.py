@@ -456,3 +456,75 @@ def test_chain_build_slot_recovers_low_rank_delta():
         if exp_best == 0:
             assert O.relative_error(res[1]["out_K"][0, 0, head], E1[0][0, 0, head]) < 1e-10
     assert (res[1]["eff_rank"][0, 0, :, :] == 2).all()   # energies 4, 1, .25: 4/5.25 < .9 <= 5/5.25
+
+
+# --------------------------------------------------------------------- R10
+def test_reuse_ratio_selection_hand_cases():
+    """Figure 5 / Tables 11-12 fix the reuse ratio rho: round(rho*S) segments
+    are reused and the largest scores fall back (ties: lower index first)."""
+    score = [0.10, 0.50, 0.30, 0.50, 0.05]
+    assert O.select_by_reuse_ratio(score, 1.0).tolist() == [False] * 5
+    assert O.select_by_reuse_ratio(score, 0.0).tolist() == [True] * 5
+    # rho 0.6 -> 3 reused, 2 fall back: the two 0.50 scores
+    assert O.select_by_reuse_ratio(score, 0.6).tolist() == [False, True, False, True, False]
+    # rho 0.8 -> 4 reused, 1 falls back: the tie at 0.50 goes to the lower index
+    assert O.select_by_reuse_ratio(score, 0.8).tolist() == [False, True, False, False, False]
+    # rho 0.5 -> round half up: 3 reused
+    assert O.select_by_reuse_ratio(score, 0.5).sum() == 2
+
+
+def test_reuse_ratio_monotone_and_exact_count():
+    rng = np.random.default_rng(20)
+    score = rng.uniform(0, 1, 37)
+    prev = None
+    for rho in np.linspace(0, 1, 21):
+        fb = O.select_by_reuse_ratio(score, rho)
+        assert fb.sum() == 37 - math.floor(rho * 37 + 0.5)
+        if prev is not None:
+            assert np.all(fb <= prev)          # a larger rho only removes fallbacks
+            # every fallback score >= every reused score
+        if fb.any() and (~fb).any():
+            assert score[fb].min() >= score[~fb].max()
+        prev = fb
+
+
+# --------------------------------------------------------------------- R11
+def test_pool_insert_fifo_and_exact_recovery():
+    """A fallback segment's dense rows yield a new anchor in slot
+    pool_next mod A (FIFO); with a delta of rank <= l the inserted state is
+    exactly dense - held, so one-hot weight on it reproduces the dense rows;
+    unflagged segments and other slots are untouched."""
+    rng = np.random.default_rng(21)
+    R, L, H, T, d, A, r, l = 1, 1, 2, 40, 8, 3, 4, 6
+    seg = O.Segments([0, 0], [2, 20], [12, 15])
+    held = [rng.standard_normal((R, L, H, T, d)) for _ in range(2)]
+    dense = []
+    for kv in range(2):
+        x = held[kv].copy()
+        for s in range(2):
+            t0, n = seg.start[s], seg.length[s]
+            for h in range(H):
+                x[0, 0, h, t0:t0 + n] += (_haar(rng, n, 2) * [1.5, 0.5]) @ _haar(rng, d, 2).T
+        dense.append(x)
+    U = [rng.standard_normal((2, L, H, 15, A, r)) for _ in range(2)]
+    W = [rng.standard_normal((2, L, H, d, A, r)) for _ in range(2)]
+    st = O.States(U[0], W[0], U[1], W[1])
+    before = st.copy()
+    summ = rng.standard_normal((2, L, H, A, d))
+    summ0 = summ.copy()
+    cursor = np.array([4, 7])
+    O.pool_insert(dense, held, seg, [False, True], cursor, st, summ, r, rng.standard_normal((d, l)), 2)
+    assert cursor.tolist() == [4, 8]                      # only the flagged segment advances
+    slot = 7 % A                                          # = 1
+    for kv in range(2):
+        assert np.array_equal(st.U[kv][0], before.U[kv][0])   # segment 0 untouched
+        for a in range(A):
+            if a != slot:
+                assert np.array_equal(st.U[kv][1, :, :, :, a], before.U[kv][1, :, :, :, a])
+        w = np.zeros((2, L, H, A))
+        w[1, :, :, slot] = 1.0
+        out = O.apply_correction((held[0], held[1]), seg, st, w)[kv]
+        t0, n = seg.start[1], seg.length[1]
+        assert O.relative_error(out[0, :, :, t0:t0 + n], dense[kv][0, :, :, t0:t0 + n]) < 1e-12
+    assert np.array_equal(summ[0], summ0[0])
+    np.testing.assert_allclose(summ[1, 0, 1, slot], held[0][0, 0, 1, 20:35].mean(axis=0), atol=1e-15)
