@@ -1,4 +1,6 @@
-// kvc_build.cu -- K1: randomized low-rank delta states (KVCMAS abstract:
+// kvc_build.cu -- K1 (FP32 path, used for f32 heads wider than 128; narrower
+// heads run the tensor-core builder in kvc_build_tc.cu): randomized low-rank
+// delta states (KVCMAS abstract:
 // compact low-rank states; listing, Figure 2 for the effective rank and
 // Figure 13 for r_Delta = 32).
 //
@@ -35,6 +37,9 @@ constexpr int kBuildThreads = 256;
 constexpr int kLMax = 64;                 // sketch width l = r + p
 constexpr int kBuildSlots = 512;          // workspace slots (max CTAs)
 constexpr int kJacobiSweeps = 14;
+// Leading dimension of the l x l work matrices in shared memory: odd, so a
+// column walk touches 32 different banks.
+constexpr int kLd = kLMax + 1;
 
 struct BuildArgs {
   const char* exact[2];
@@ -59,7 +64,7 @@ struct BuildArgs {
 template <typename T>
 __device__ __forceinline__ float ld_elem(const T* p);
 template <>
-__device__ __forceinline__ float ld_elem<float>(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float ld_elem<float>(const float* p) { return *p; }
 template <>
 __device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16* p) {
   return __bfloat162float(*p);
@@ -147,8 +152,8 @@ __device__ void gram(const float* M, int m, int l, float* G) {
     const int j = i + rem;
     float acc = 0.0f;
     for (int t = 0; t < m; ++t) acc = fmaf(M[t * l + i], M[t * l + j], acc);
-    G[i * kLMax + j] = acc;
-    G[j * kLMax + i] = acc;
+    G[i * kLd + j] = acc;
+    G[j * kLd + i] = acc;
   }
 }
 
@@ -160,26 +165,26 @@ __device__ void cholqr_pass(float* M, int m, int l, float* G, float* R, int* kee
   __syncthreads();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    // R upper triangular, row-major with stride kLMax; column j computed in order.
+    // R upper triangular, row-major with stride kLd; column j computed in order.
     for (int j = 0; j < l; ++j) {
       float s = 0.0f;
-      for (int i = lane; i < j; i += 32) s += R[i * kLMax + j] * R[i * kLMax + j];
+      for (int i = lane; i < j; i += 32) s += R[i * kLd + j] * R[i * kLd + j];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      const float gjj = G[j * kLMax + j];
+      const float gjj = G[j * kLd + j];
       const float piv = gjj - s;
       const bool ok = gjj > 0.0f && piv > 1e-6f * gjj;
       const float rjj = ok ? sqrtf(piv) : 0.0f;
       if (lane == 0) {
-        R[j * kLMax + j] = rjj;
+        R[j * kLd + j] = rjj;
         keep[j] = ok ? 1 : 0;
       }
       __syncwarp();
       // R[j, k] for k > j: (G[j,k] - sum_{i<j} R[i,j] R[i,k]) / R[j,j]
       for (int k = j + 1 + lane; k < l; k += 32) {
-        float v = G[j * kLMax + k];
-        for (int i = 0; i < j; ++i) v -= R[i * kLMax + j] * R[i * kLMax + k];
-        R[j * kLMax + k] = ok ? v / rjj : 0.0f;
+        float v = G[j * kLd + k];
+        for (int i = 0; i < j; ++i) v -= R[i * kLd + j] * R[i * kLd + k];
+        R[j * kLd + k] = ok ? v / rjj : 0.0f;
       }
       __syncwarp();
     }
@@ -191,8 +196,8 @@ __device__ void cholqr_pass(float* M, int m, int l, float* G, float* R, int* kee
     float* row = M + t * l;
     for (int j = 0; j < l; ++j) {
       float v = row[j];
-      for (int i = 0; i < j; ++i) v = fmaf(-row[i], R[i * kLMax + j], v);
-      row[j] = keep[j] ? v / R[j * kLMax + j] : 0.0f;
+      for (int i = 0; i < j; ++i) v = fmaf(-row[i], R[i * kLd + j], v);
+      row[j] = keep[j] ? v / R[j * kLd + j] : 0.0f;
     }
   }
   __syncthreads();
@@ -203,18 +208,37 @@ __device__ void orth(float* M, int m, int l, float* G, float* R, int* keep) {
   cholqr_pass(M, m, l, G, R, keep);
 }
 
-// Parallel cyclic Jacobi on the symmetric l x l matrix A (stride kLMax):
+// Parallel cyclic Jacobi on the symmetric l x l matrix A (stride kLd):
 // on return A is (numerically) diagonal and V holds the eigenvectors as
 // columns.  Round-robin pairing over an even number of indices (a dummy index
 // pads odd l).
-__device__ void jacobi_eigen(float* A, float* V, int l, float* cs, int* pairs) {
+__device__ void jacobi_eigen(float* A, float* V, int l, float* cs, int* pairs, float* red) {
   const int n = (l + 1) & ~1;
-  for (int idx = threadIdx.x; idx < kLMax * kLMax; idx += kBuildThreads) {
-    const int i = idx / kLMax, j = idx % kLMax;
+  for (int idx = threadIdx.x; idx < kLMax * kLd; idx += kBuildThreads) {
+    const int i = idx / kLd, j = idx % kLd;
     V[idx] = (i == j) ? 1.0f : 0.0f;
   }
   __syncthreads();
+  float prev_off = 0.0f;
   for (int sweep = 0; sweep < kJacobiSweeps; ++sweep) {
+    // stop once the off-diagonal energy is at fp32 rounding level (the
+    // decision is uniform: every thread sees the same fixed-order sums)
+    float off = 0.0f, dia = 0.0f;
+    for (int idx = threadIdx.x; idx < l * l; idx += kBuildThreads) {
+      const int i = idx / l, j = idx % l;
+      const float v = A[i * kLd + j];
+      if (i == j)
+        dia = fmaf(v, v, dia);
+      else
+        off = fmaf(v, v, off);
+    }
+    off = block_sum(off, red);
+    dia = block_sum(dia, red);
+    // converged: negligible, or already small and no longer shrinking (the
+    // fp32 rounding floor)
+    if (!(off > 1e-12f * dia)) break;
+    if (sweep > 0 && off <= 1e-8f * dia && off > 0.25f * prev_off) break;
+    prev_off = off;
     for (int round = 0; round < n - 1; ++round) {
       // pair k: (a, b) from the circle method with index n-1 fixed
       if (threadIdx.x < n / 2) {
@@ -234,9 +258,9 @@ __device__ void jacobi_eigen(float* A, float* V, int l, float* cs, int* pairs) {
         }
         float c = 1.0f, s = 0.0f;
         if (b < l) {
-          const float apq = A[a * kLMax + b];
+          const float apq = A[a * kLd + b];
           if (apq != 0.0f) {
-            const float app = A[a * kLMax + a], aqq = A[b * kLMax + b];
+            const float app = A[a * kLd + a], aqq = A[b * kLd + b];
             const float theta = (aqq - app) / (2.0f * apq);
             const float tt = copysignf(1.0f, theta) / (fabsf(theta) + sqrtf(theta * theta + 1.0f));
             c = rsqrtf(tt * tt + 1.0f);
@@ -255,9 +279,9 @@ __device__ void jacobi_eigen(float* A, float* V, int l, float* cs, int* pairs) {
         const int a = pairs[2 * k], b = pairs[2 * k + 1];
         if (b >= l) continue;
         const float c = cs[2 * k], s = cs[2 * k + 1];
-        const float x = A[a * kLMax + j], y = A[b * kLMax + j];
-        A[a * kLMax + j] = c * x - s * y;
-        A[b * kLMax + j] = s * x + c * y;
+        const float x = A[a * kLd + j], y = A[b * kLd + j];
+        A[a * kLd + j] = c * x - s * y;
+        A[b * kLd + j] = s * x + c * y;
       }
       __syncthreads();
       // columns: A <- A J, V <- V J
@@ -266,12 +290,12 @@ __device__ void jacobi_eigen(float* A, float* V, int l, float* cs, int* pairs) {
         const int a = pairs[2 * k], b = pairs[2 * k + 1];
         if (b >= l) continue;
         const float c = cs[2 * k], s = cs[2 * k + 1];
-        const float x = A[i * kLMax + a], y = A[i * kLMax + b];
-        A[i * kLMax + a] = c * x - s * y;
-        A[i * kLMax + b] = s * x + c * y;
-        const float vx = V[i * kLMax + a], vy = V[i * kLMax + b];
-        V[i * kLMax + a] = c * vx - s * vy;
-        V[i * kLMax + b] = s * vx + c * vy;
+        const float x = A[i * kLd + a], y = A[i * kLd + b];
+        A[i * kLd + a] = c * x - s * y;
+        A[i * kLd + b] = s * x + c * y;
+        const float vx = V[i * kLd + a], vy = V[i * kLd + b];
+        V[i * kLd + a] = c * vx - s * vy;
+        V[i * kLd + b] = s * vx + c * vy;
       }
       __syncthreads();
     }
@@ -283,9 +307,9 @@ __global__ void __launch_bounds__(kBuildThreads)
     build_simt_kernel(const BuildArgs a, const __grid_constant__ SegTable seg) {
   extern __shared__ float bsm[];
   float* X = bsm;                               // d x l   (Omega, Z, B^T)
-  float* G = X + a.d * a.l;                     // kLMax x kLMax
-  float* R = G + kLMax * kLMax;                 // kLMax x kLMax (also Jacobi V)
-  float* cs = R + kLMax * kLMax;                // 2 * kLMax
+  float* G = X + a.d * a.l;                     // kLMax x kLd
+  float* R = G + kLMax * kLd;                   // kLMax x kLd (also Jacobi V)
+  float* cs = R + kLMax * kLd;                  // 2 * kLMax
   float* lam = cs + 2 * kLMax;                  // kLMax
   float* red = lam + kLMax;                     // 32
   int* keep = reinterpret_cast<int*>(red + 32); // kLMax
@@ -315,11 +339,23 @@ __global__ void __launch_bounds__(kBuildThreads)
     // ---- delta = exact - ref (fp32) and |delta|_F^2
     __syncthreads();
     float ss = 0.0f;
-    for (int idx = threadIdx.x; idx < n * d; idx += kBuildThreads) {
-      const int t = idx / d, c = idx % d;
-      const float v = ld_elem<T>(ex + t * a.es[kv][3] + c) - ld_elem<T>(rf + t * a.rs[kv][3] + c);
-      Dw[idx] = v;
-      ss = fmaf(v, v, ss);
+    {
+      constexpr int VEC = 16 / sizeof(T);        // elements per 16-byte load
+      const int vpr = d / VEC;
+      for (int idx = threadIdx.x; idx < n * vpr; idx += kBuildThreads) {
+        const int t = idx / vpr, c = (idx % vpr) * VEC;
+        const uint4 xe = *reinterpret_cast<const uint4*>(ex + t * a.es[kv][3] + c);
+        const uint4 xr = *reinterpret_cast<const uint4*>(rf + t * a.rs[kv][3] + c);
+        const T* pe = reinterpret_cast<const T*>(&xe);
+        const T* pr = reinterpret_cast<const T*>(&xr);
+        float* drow = Dw + static_cast<int64_t>(t) * d + c;
+#pragma unroll
+        for (int u = 0; u < VEC; ++u) {
+          const float v = ld_elem<T>(pe + u) - ld_elem<T>(pr + u);
+          drow[u] = v;
+          ss = fmaf(v, v, ss);
+        }
+      }
     }
     const float total = block_sum(ss, red);
     if (a.summaries != nullptr && kv == 0) {
@@ -349,8 +385,8 @@ __global__ void __launch_bounds__(kBuildThreads)
     // ---- small SVD of B through the eigen-decomposition of B B^T
     gram(X, d, l, G);                           // G = (B^T)^T B^T = B B^T
     __syncthreads();
-    jacobi_eigen(G, R, l, cs, pairs);           // R = eigenvectors
-    for (int i = threadIdx.x; i < l; i += kBuildThreads) lam[i] = fmaxf(G[i * kLMax + i], 0.0f);
+    jacobi_eigen(G, R, l, cs, pairs, red);      // R = eigenvectors
+    for (int i = threadIdx.x; i < l; i += kBuildThreads) lam[i] = fmaxf(G[i * kLd + i], 0.0f);
     __syncthreads();
     for (int i = threadIdx.x; i < l; i += kBuildThreads) {
       int rank = 0;
@@ -377,18 +413,28 @@ __global__ void __launch_bounds__(kBuildThreads)
 
     // ---- U = Q Ub_r diag(sigma_r): rows of the segment, zero padding up to Tmax
     T* Uo = reinterpret_cast<T*>(a.U[kv]) + static_cast<int64_t>(unit) * a.Tmax * a.A * a.r;
-    for (int idx = threadIdx.x; idx < a.Tmax * a.r; idx += kBuildThreads) {
-      const int t = idx / a.r, j = idx % a.r;
-      float v = 0.0f;
-      if (t < n && j < l) {
-        const int col = order[j];
-        const float sj = sqrtf(lam[col]);
-        const float* qrow = Qw + static_cast<int64_t>(t) * l;
-        float acc = 0.0f;
-        for (int i = 0; i < l; ++i) acc = fmaf(qrow[i], R[i * kLMax + col], acc);
-        v = acc * sj;
+    for (int t = threadIdx.x; t < a.Tmax; t += kBuildThreads) {
+      T* urow = Uo + static_cast<int64_t>(t) * a.A * a.r + slot * a.r;
+      if (t >= n) {
+        for (int j = 0; j < a.r; ++j) st_elem<T>(urow + j, 0.0f);
+        continue;
       }
-      st_elem<T>(Uo + (static_cast<int64_t>(t) * a.A + slot) * a.r + j, v);
+      float qv[kLMax];
+      const float* qrow = Qw + static_cast<int64_t>(t) * l;
+#pragma unroll
+      for (int i = 0; i < kLMax; ++i) qv[i] = (i < l) ? qrow[i] : 0.0f;
+      for (int j = 0; j < a.r; ++j) {
+        float v = 0.0f;
+        if (j < l) {
+          const int col = order[j];
+          float acc = 0.0f;
+#pragma unroll
+          for (int i = 0; i < kLMax; ++i)
+            if (i < l) acc = fmaf(qv[i], R[i * kLd + col], acc);
+          v = acc * sqrtf(lam[col]);
+        }
+        st_elem<T>(urow + j, v);
+      }
     }
     // ---- W = B^T Ub_r diag(1 / sigma_r) (zero for negligible sigma)
     T* Wo = reinterpret_cast<T*>(a.W[kv]) + static_cast<int64_t>(unit) * d * a.A * a.r;
@@ -400,7 +446,7 @@ __global__ void __launch_bounds__(kBuildThreads)
         const float sj = sqrtf(lam[col]);
         if (sj > 1e-6f * sig_max && sj > 0.0f) {
           float acc = 0.0f;
-          for (int i = 0; i < l; ++i) acc = fmaf(X[c * l + i], R[i * kLMax + col], acc);
+          for (int i = 0; i < l; ++i) acc = fmaf(X[c * l + i], R[i * kLd + col], acc);
           v = acc / sj;
         }
       }
@@ -423,6 +469,7 @@ int64_t slot_floats(const Dims& dm, int l) {
 size_t build_workspace_bytes(const Dims& dm, int l) {
   const int64_t mats = dm.units() * 2;
   if (mats <= 0) return 0;
+  if (build_tc_supported(dm, l)) return 0;      // the tensor-core builder keeps all on chip
   const int64_t slots = mats < kBuildSlots ? mats : kBuildSlots;
   return static_cast<size_t>(slots * slot_floats(dm, l) * static_cast<int64_t>(sizeof(float)));
 }
@@ -433,6 +480,9 @@ cudaError_t launch_build(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
                          float* sigma, int32_t* eff_rank, void* workspace, int32_t* dev_status,
                          cudaStream_t stream, const uint8_t* seg_mask, const int32_t* seg_slot,
                          float* summaries) {
+  if (build_tc_supported(dm, l))
+    return launch_build_tc(dm, seg, dtype, exactv, refv, omega, l, q, energy_frac, slot, U, W,
+                           sigma, eff_rank, dev_status, stream, seg_mask, seg_slot, summaries);
   (void)dev_status;
   BuildArgs a{};
   a.seg_mask = seg_mask;
@@ -472,7 +522,7 @@ cudaError_t launch_build(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
   if (mats > 0x7FFFFFFF) return cudaErrorInvalidValue;
   a.n_mats = static_cast<int32_t>(mats);
   const int grid = static_cast<int>(mats < kBuildSlots ? mats : kBuildSlots);
-  const size_t smem = (static_cast<size_t>(dm.d) * l + 2 * kLMax * kLMax + 4 * kLMax + 32) *
+  const size_t smem = (static_cast<size_t>(dm.d) * l + 2 * kLMax * kLd + 4 * kLMax + 32) *
                           sizeof(float) +
                       4 * kLMax * sizeof(int);
   cudaError_t e;

@@ -95,6 +95,16 @@ cudaError_t launch_build(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
                          cudaStream_t stream, const uint8_t* seg_mask = nullptr,
                          const int32_t* seg_slot = nullptr, float* summaries = nullptr);
 
+// K1 on tcgen05 (d <= 128, l <= 64): M = delta^T delta on tensor cores, the
+// subspace iteration on the feature side; needs no workspace.
+bool build_tc_supported(const Dims& dm, int l);
+cudaError_t launch_build_tc(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
+                            const View exactv[2], const View refv[2], const float* omega, int l,
+                            int q, float energy_frac, int slot, void* U[2], void* W[2],
+                            float* sigma, int32_t* eff_rank, int32_t* dev_status,
+                            cudaStream_t stream, const uint8_t* seg_mask, const int32_t* seg_slot,
+                            float* summaries);
+
 // Anchor pool: pool_next[s] += 1 for every flagged segment.
 cudaError_t launch_pool_advance(const Dims& dm, const uint8_t* fallback, int32_t* pool_next,
                                 cudaStream_t stream);

@@ -322,9 +322,12 @@ def run_kvc(args, wl):
         gemm_flop = 0
         for s in range(wl.S):
             gemm_flop += wl.L * wl.H * 2 * 2 * (2 * wl.power_iters + 2) * wl.seg_len[s] * wl.d * wl.l
-        builder = {"kernel": "build_simt_kernel", "launch_ms": b_ms, "matrices": mats,
-                   "gemm_tflops": gemm_flop / (b_ms / 1000.0) / 1e12,
-                   "tensor_pipe": "not used (FP32 FMA builder)"}
+        tc = wl.d <= 128 and wl.l <= 64
+        builder = {"kernel": "build_tc_kernel" if tc else "build_simt_kernel",
+                   "launch_ms": b_ms, "matrices": mats,
+                   "hmt_gemm_equivalent_tflops": gemm_flop / (b_ms / 1000.0) / 1e12,
+                   "tensor_path": ("M = delta^T delta on tcgen05 (split bf16)" if tc
+                                   else "FP32 FMA")}
 
     # ---- end to end through the C ABI with host buffers
     e2e = None

@@ -40,6 +40,8 @@ def _cases():
                                       fallback_frac=0.34),
         "d64-bf16": synth.scaled(LC, L=1, H=2, R=1, seg_len=[300, 64], d=64, A=4, r=24,
                                  oversample=8, fallback_frac=0.0),
+        # f32 head wider than the tensor-core builder's 128 rows: FP32 builder
+        "f32-d256": synth.scaled(tiny, L=1, H=1, R=1, seg_len=[200], d=256),
     }
 
 
