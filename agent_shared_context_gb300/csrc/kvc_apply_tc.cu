@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_alloc<kTmemCols>(&bars->tmem_base);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -522,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc<kTmemCols>(tmem);
 }
 
 template <int D>

@@ -103,104 +103,146 @@ __device__ __forceinline__ float blk_sum(float v, float* red) {
 }
 
 // C[m x n] = op(A) B with op(A) = A (m x k, row stride lda) or A^T (A is
-// k x m).  B is k x n (row stride ldb).  All operands in shared memory.
+// k x m).  B is k x n (row stride ldb).  All operands in shared memory.  When
+// n and ldb are multiples of 4 each thread computes four adjacent outputs
+// from float4 loads of B.
 __device__ void mm(const float* A, int lda, bool transA, const float* B, int ldb, float* C,
                    int ldc, int m, int k, int n) {
   __syncthreads();
-  for (int idx = threadIdx.x; idx < m * n; idx += kTcThreads) {
-    const int i = idx / n, j = idx % n;
-    float acc = 0.0f;
-    if (transA) {
-      for (int t = 0; t < k; ++t) acc = fmaf(A[t * lda + i], B[t * ldb + j], acc);
-    } else {
-      for (int t = 0; t < k; ++t) acc = fmaf(A[i * lda + t], B[t * ldb + j], acc);
+  if ((n & 3) == 0 && (ldb & 3) == 0) {
+    const int n4 = n >> 2;
+    for (int idx = threadIdx.x; idx < m * n4; idx += kTcThreads) {
+      const int i = idx / n4, j = (idx % n4) * 4;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int t = 0; t < k; ++t) {
+        const float a = transA ? A[t * lda + i] : A[i * lda + t];
+        const float4 b = *reinterpret_cast<const float4*>(B + t * ldb + j);
+        acc.x = fmaf(a, b.x, acc.x);
+        acc.y = fmaf(a, b.y, acc.y);
+        acc.z = fmaf(a, b.z, acc.z);
+        acc.w = fmaf(a, b.w, acc.w);
+      }
+      float* c = C + i * ldc + j;
+      c[0] = acc.x;
+      c[1] = acc.y;
+      c[2] = acc.z;
+      c[3] = acc.w;
     }
-    C[i * ldc + j] = acc;
-  }
-  __syncthreads();
-}
-
-// Upper-triangular R with G = R^T R (left-looking, one warp).  A pivot below
-// 1e-6 of its column's squared norm marks a dependent column: keep[j] = 0 and
-// row j of R is zero.  ld is the row stride of G and R.
-__device__ void chol(const float* G, float* R, int* keep, int l, int ld) {
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    for (int j = 0; j < l; ++j) {
-      float s = 0.0f;
-      for (int i = lane; i < j; i += 32) s = fmaf(R[i * ld + j], R[i * ld + j], s);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      const float gjj = G[j * ld + j];
-      const float piv = gjj - s;
-      const bool ok = gjj > 0.0f && piv > 1e-6f * gjj;
-      const float rjj = ok ? sqrtf(piv) : 0.0f;
-      for (int k = j + 1 + lane; k < l; k += 32) {
-        float v = G[j * ld + k];
-        for (int i = 0; i < j; ++i) v = fmaf(-R[i * ld + j], R[i * ld + k], v);
-        R[j * ld + k] = ok ? v / rjj : 0.0f;
-      }
-      if (lane == 0) {
-        R[j * ld + j] = rjj;
-        keep[j] = ok ? 1 : 0;
-      }
-      for (int k = lane; k < j; k += 32) R[j * ld + k] = 0.0f;   // strictly lower part
-      __syncwarp();
+  } else {
+    for (int idx = threadIdx.x; idx < m * n; idx += kTcThreads) {
+      const int i = idx / n, j = idx % n;
+      float acc = 0.0f;
+      for (int t = 0; t < k; ++t)
+        acc = fmaf(transA ? A[t * lda + i] : A[i * lda + t], B[t * ldb + j], acc);
+      C[i * ldc + j] = acc;
     }
   }
   __syncthreads();
 }
 
-// Ri = R^-1 for upper-triangular R, with the rows and columns of dropped
-// indices zero (so Y Ri zeroes the dependent columns).  Thread j solves
-// column j by back substitution.
-__device__ void tri_inv(const float* R, const int* keep, float* Ri, int l, int ld) {
+// Upper-triangular R (row stride ls) with G = R^T R: right-looking over the
+// whole CTA with one barrier per column.  The trailing update uses the
+// unscaled pivot row (R[i][k] -= R[j][i] R[j][k] / pivot_j) so the rows can
+// be scaled once at the end.  `pairs_ik` lists the (i, k <= l) index pairs of
+// the upper triangle, i in the high byte.  A pivot below 1e-6 of its
+// column's squared norm marks a dependent column: keep[j] = 0, row j zero.
+__device__ void chol(const float* G, float* R, int* keep, float* dinv,
+                     const uint16_t* pairs_ik, int l, int ls) {
   __syncthreads();
-  for (int idx = threadIdx.x; idx < l * l; idx += kTcThreads) Ri[(idx / l) * ld + idx % l] = 0.0f;
+  const int npairs = l * (l + 1) / 2;
+  for (int idx = threadIdx.x; idx < l * l; idx += kTcThreads) {
+    const int i = idx / l, k = idx % l;
+    R[i * ls + k] = (k >= i) ? G[i * ls + k] : 0.0f;
+  }
   __syncthreads();
-  for (int j = threadIdx.x; j < l; j += kTcThreads) {
-    if (!keep[j]) continue;
-    Ri[j * ld + j] = 1.0f / R[j * ld + j];
-    for (int i = j - 1; i >= 0; --i) {
-      if (!keep[i]) continue;
-      float s = 0.0f;
-      for (int k = i + 1; k <= j; ++k) s = fmaf(R[i * ld + k], Ri[k * ld + j], s);
-      Ri[i * ld + j] = -s / R[i * ld + i];
+  for (int j = 0; j < l; ++j) {
+    const float gjj = G[j * ls + j];
+    const float piv = R[j * ls + j];
+    const bool ok = gjj > 0.0f && piv > 1e-6f * gjj;
+    const float inv2 = ok ? 1.0f / piv : 0.0f;
+    if (threadIdx.x == 0) {
+      keep[j] = ok ? 1 : 0;
+      dinv[j] = ok ? rsqrtf(piv) : 0.0f;
     }
+    for (int p = threadIdx.x; p < npairs; p += kTcThreads) {
+      const int i = pairs_ik[p] >> 8, k = pairs_ik[p] & 255;
+      if (i > j) R[i * ls + k] = fmaf(-R[j * ls + i] * inv2, R[j * ls + k], R[i * ls + k]);
+    }
+    __syncthreads();
+  }
+  for (int p = threadIdx.x; p < npairs; p += kTcThreads) {
+    const int i = pairs_ik[p] >> 8, k = pairs_ik[p] & 255;
+    R[i * ls + k] *= dinv[i];
+  }
+  __syncthreads();
+}
+
+// Ri = R^-1 (row stride lr) for upper-triangular R (row stride ls): back
+// substitution, right-looking over the CTA (B = I; for i = l-1 .. 0 the
+// final row i is B[i] / R_ii and it is eliminated from the rows above), one
+// barrier per row; rows are scaled at the end.  Rows and columns of dropped
+// indices stay zero, so Y Ri zeroes the dependent columns.
+__device__ void tri_inv(const float* R, const int* keep, float* Ri, int l, int ls, int lr) {
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < l * lr; idx += kTcThreads) {
+    const int i = idx / lr, j = idx % lr;
+    Ri[idx] = (i == j && keep[i]) ? 1.0f : 0.0f;
+  }
+  __syncthreads();
+  // fixed thread mapping (l <= 64): column offset tx, row phase ty
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
+  for (int i = l - 1; i > 0; --i) {
+    const float inv = keep[i] ? 1.0f / R[i * ls + i] : 0.0f;
+    const int col = i + tx;                          // X[i][col] is zero for col < i
+    if (col < l) {
+      const float xi = Ri[i * lr + col] * inv;
+      for (int m = ty; m < i; m += kTcThreads / 64)
+        Ri[m * lr + col] = fmaf(-R[m * ls + i], xi, Ri[m * lr + col]);
+    }
+    __syncthreads();
+  }
+  for (int idx = threadIdx.x; idx < l * l; idx += kTcThreads) {
+    const int i = idx / l, j = idx % l;
+    Ri[i * lr + j] *= keep[i] ? 1.0f / R[i * ls + i] : 0.0f;
   }
   __syncthreads();
 }
 
 // Parallel cyclic Jacobi (round-robin pairing) on the symmetric l x l matrix
-// A (row stride ld): on return diag(A) holds the eigenvalues and V the
-// eigenvectors as columns.  Stops once the off-diagonal energy is negligible
-// or, already small, stops shrinking (the fp32 rounding floor).
-__device__ void jacobi(float* A, float* V, int l, int ld, float* cs, int* pairs, float* red) {
+// A (row stride ls) over the CTA: on return diag(A) holds the eigenvalues
+// and V the eigenvectors as columns.  Each round rotates n/2 disjoint pairs;
+// A' = J^T A J is applied block-wise (thread = one 2x2 block (p,q) x (p',q'),
+// both sides at once, so one barrier suffices) and V' = V J alongside.  A
+// pair is rotated only while |a_pq| > max(1e-7 sqrt(|a_pp a_qq|),
+// 2e-7 max|a_ii|) -- the absolute floor sits above fp32 rounding noise -- and
+// the solver stops after the first sweep that rotates nothing (or kSweeps).
+__device__ void jacobi(float* A, float* V, int l, int ls, float* cs, int* pairs, float* red,
+                       uint16_t* items) {
   const int n = (l + 1) & ~1;
+  const int np = n / 2;
+  // item table (no divisions in the rounds): A blocks (u, v) then V entries (k, i)
+  for (int idx = threadIdx.x; idx < np * np + np * l; idx += kTcThreads)
+    items[idx] = idx < np * np ? static_cast<uint16_t>(((idx / np) << 8) | (idx % np))
+                               : static_cast<uint16_t>((((idx - np * np) / l) << 8) |
+                                                       ((idx - np * np) % l));
   for (int idx = threadIdx.x; idx < l * l; idx += kTcThreads) {
     const int i = idx / l, j = idx % l;
-    V[i * ld + j] = (i == j) ? 1.0f : 0.0f;
+    V[i * ls + j] = (i == j) ? 1.0f : 0.0f;
   }
   __syncthreads();
-  float prev_off = 0.0f;
   for (int sweep = 0; sweep < kSweeps; ++sweep) {
-    float off = 0.0f, dia = 0.0f;
-    for (int idx = threadIdx.x; idx < l * l; idx += kTcThreads) {
-      const int i = idx / l, j = idx % l;
-      const float v = A[i * ld + j];
-      if (i == j)
-        dia = fmaf(v, v, dia);
-      else
-        off = fmaf(v, v, off);
-    }
-    off = blk_sum(off, red);
-    dia = blk_sum(dia, red);
-    if (!(off > 1e-12f * dia)) break;
-    if (sweep > 0 && off <= 1e-8f * dia && off > 0.25f * prev_off) break;
-    prev_off = off;
+    float dmax = 0.0f;
+    for (int i = threadIdx.x; i < l; i += kTcThreads) dmax = fmaxf(dmax, fabsf(A[i * ls + i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = dmax;
+    __syncthreads();
+    dmax = 0.0f;
+    for (int w = 0; w < kTcThreads / 32; ++w) dmax = fmaxf(dmax, red[w]);
+    const float abs_tol = 2e-7f * dmax;
+    int rotated = 0;
     for (int round = 0; round < n - 1; ++round) {
-      if (threadIdx.x < n / 2) {
+      if (threadIdx.x < np) {
         const int k = threadIdx.x;
         int a, b;
         if (k == 0) {
@@ -215,65 +257,81 @@ __device__ void jacobi(float* A, float* V, int l, int ld, float* cs, int* pairs,
           a = b;
           b = t;
         }
-        float c = 1.0f, s = 0.0f;
+        float c = 1.0f, sn = 0.0f;
         if (b < l) {
-          const float apq = A[a * ld + b];
-          if (apq != 0.0f) {
-            const float app = A[a * ld + a], aqq = A[b * ld + b];
+          const float apq = A[a * ls + b];
+          const float app = A[a * ls + a], aqq = A[b * ls + b];
+          const float tol = fmaxf(1e-7f * sqrtf(fabsf(app * aqq)), abs_tol);
+          if (fabsf(apq) > tol) {
             const float theta = (aqq - app) / (2.0f * apq);
             const float tt = copysignf(1.0f, theta) / (fabsf(theta) + sqrtf(theta * theta + 1.0f));
             c = rsqrtf(tt * tt + 1.0f);
-            s = tt * c;
+            sn = tt * c;
+            rotated = 1;
           }
         }
         pairs[2 * k] = a;
         pairs[2 * k + 1] = b;
         cs[2 * k] = c;
-        cs[2 * k + 1] = s;
+        cs[2 * k + 1] = sn;
       }
       __syncthreads();
-      for (int idx = threadIdx.x; idx < (n / 2) * l; idx += kTcThreads) {
-        const int k = idx / l, j = idx % l;
-        const int a = pairs[2 * k], b = pairs[2 * k + 1];
-        if (b >= l) continue;
-        const float c = cs[2 * k], s = cs[2 * k + 1];
-        const float x = A[a * ld + j], y = A[b * ld + j];
-        A[a * ld + j] = c * x - s * y;
-        A[b * ld + j] = s * x + c * y;
-      }
-      __syncthreads();
-      for (int idx = threadIdx.x; idx < (n / 2) * l; idx += kTcThreads) {
-        const int k = idx / l, i = idx % l;
-        const int a = pairs[2 * k], b = pairs[2 * k + 1];
-        if (b >= l) continue;
-        const float c = cs[2 * k], s = cs[2 * k + 1];
-        const float x = A[i * ld + a], y = A[i * ld + b];
-        A[i * ld + a] = c * x - s * y;
-        A[i * ld + b] = s * x + c * y;
-        const float vx = V[i * ld + a], vy = V[i * ld + b];
-        V[i * ld + a] = c * vx - s * vy;
-        V[i * ld + b] = s * vx + c * vy;
+      // A blocks: rows of pair u, columns of pair v (dummy index n-1 >= l skipped)
+      for (int idx = threadIdx.x; idx < np * np + np * l; idx += kTcThreads) {
+        const int it8 = items[idx] >> 8, itl = items[idx] & 255;
+        if (idx < np * np) {
+          const int u = it8, v = itl;
+          const int a = pairs[2 * u], b = pairs[2 * u + 1];
+          const int a2 = pairs[2 * v], b2 = pairs[2 * v + 1];
+          const float cu = cs[2 * u], su = cs[2 * u + 1];
+          const float cv = cs[2 * v], sv = cs[2 * v + 1];
+          if (su == 0.0f && sv == 0.0f) continue;
+          const bool rb = b < l, cb = b2 < l;
+          const float x00 = A[a * ls + a2];
+          const float x01 = cb ? A[a * ls + b2] : 0.0f;
+          const float x10 = rb ? A[b * ls + a2] : 0.0f;
+          const float x11 = (rb && cb) ? A[b * ls + b2] : 0.0f;
+          // left: J_u^T (rows a, b)
+          const float y00 = cu * x00 - su * x10, y01 = cu * x01 - su * x11;
+          const float y10 = su * x00 + cu * x10, y11 = su * x01 + cu * x11;
+          // right: J_v (columns a2, b2)
+          A[a * ls + a2] = cv * y00 - sv * y01;
+          if (cb) A[a * ls + b2] = sv * y00 + cv * y01;
+          if (rb) A[b * ls + a2] = cv * y10 - sv * y11;
+          if (rb && cb) A[b * ls + b2] = sv * y10 + cv * y11;
+        } else {
+          const int k = it8, i = itl;
+          const int a = pairs[2 * k], b = pairs[2 * k + 1];
+          const float sn = cs[2 * k + 1];
+          if (b >= l || sn == 0.0f) continue;
+          const float c = cs[2 * k];
+          const float vx = V[i * ls + a], vy = V[i * ls + b];
+          V[i * ls + a] = c * vx - sn * vy;
+          V[i * ls + b] = sn * vx + c * vy;
+        }
       }
       __syncthreads();
     }
+    if (!__syncthreads_or(rotated)) break;
   }
   __syncthreads();
 }
 
 // out[c, j] = sum_k M[c, k] X[k, j] for the kDP feature rows c, with M in
 // TMEM (lane = row c, column = k).  Two warps per TMEM lane quadrant split
-// the l output columns.  X and out are kDP x l, row stride l.
-__device__ void tmem_mx(uint32_t tmem, const float* X, float* out, int d, int l) {
+// the lp output columns in float4 groups.  X and out: kDP x lp (stride lp,
+// lp a multiple of 4).
+__device__ void tmem_mx(uint32_t tmem, const float* X, float* out, int d, int lp) {
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qd = warp & 3, half = warp >> 2;
   const int c = qd * 32 + lane;
-  const int lh = (l + 1) / 2;
+  const int lh = (((lp >> 1) + 3) >> 2) << 2;
   const int j0 = half * lh;
-  const int nj = min(lh, l - j0);
-  float acc[kLmax / 2];
+  const int nj = min(lh, lp - j0);                   // multiple of 4, may be <= 0
+  float4 acc[kLmax / 8];
 #pragma unroll
-  for (int jj = 0; jj < kLmax / 2; ++jj) acc[jj] = 0.0f;
+  for (int q4 = 0; q4 < kLmax / 8; ++q4) acc[q4] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   tc_fence_after();
   for (int kb = 0; kb < kDP / 32; ++kb) {
     uint32_t v[32];
@@ -287,78 +345,87 @@ __device__ void tmem_mx(uint32_t tmem, const float* X, float* out, int d, int l)
       const int k = kb * 32 + kk;
       if (k < d) {
         const float m = __uint_as_float(v[kk]);
-        const float* xr = X + k * l + j0;
+        const float* xr = X + k * lp + j0;
 #pragma unroll
-        for (int jj = 0; jj < kLmax / 2; ++jj)
-          if (jj < nj) acc[jj] = fmaf(m, xr[jj], acc[jj]);
+        for (int q4 = 0; q4 < kLmax / 8; ++q4) {
+          if (4 * q4 < nj) {
+            const float4 x = *reinterpret_cast<const float4*>(xr + 4 * q4);
+            acc[q4].x = fmaf(m, x.x, acc[q4].x);
+            acc[q4].y = fmaf(m, x.y, acc[q4].y);
+            acc[q4].z = fmaf(m, x.z, acc[q4].z);
+            acc[q4].w = fmaf(m, x.w, acc[q4].w);
+          }
+        }
       }
     }
   }
 #pragma unroll
-  for (int jj = 0; jj < kLmax / 2; ++jj)
-    if (jj < nj) out[c * l + j0 + jj] = acc[jj];
+  for (int q4 = 0; q4 < kLmax / 8; ++q4)
+    if (4 * q4 < nj) *reinterpret_cast<float4*>(out + c * lp + j0 + 4 * q4) = acc[q4];
   tc_fence_before();
   __syncthreads();
 }
 
-// Z <- Z R^-1 with R from CholeskyQR of Z (rows x l), twice (CholeskyQR2).
-// G, R, Ri: l x l (stride ld); T: rows x l scratch.
-__device__ void orth2(float* Z, float* T, int rows, int l, int ld, float* G, float* R, float* Ri,
-                      int* keep) {
-  for (int pass = 0; pass < 2; ++pass) {
-    mm(Z, l, true, Z, l, G, ld, l, rows, l);        // G = Z^T Z
-    chol(G, R, keep, l, ld);
-    tri_inv(R, keep, Ri, l, ld);
-    mm(Z, l, false, Ri, ld, T, l, rows, l, l);      // T = Z Ri
-    for (int idx = threadIdx.x; idx < rows * l; idx += kTcThreads) Z[idx] = T[idx];
-    __syncthreads();
-  }
+// One CholeskyQR pass on Z (rows x lp, stride lp): Z <- Z R^-1 (through T).
+__device__ void orth1(float* Z, float* T, int rows, int l, int lp, int ls, float* G, float* R,
+                      float* Ri, int* keep, float* dinv, const uint16_t* pik) {
+  mm(Z, lp, true, Z, lp, G, ls, l, rows, l);         // G = Z^T Z
+  chol(G, R, keep, dinv, pik, l, ls);
+  tri_inv(R, keep, Ri, l, ls, lp);
+  mm(Z, lp, false, Ri, lp, T, lp, rows, l, lp);      // T = Z Ri
+  for (int idx = threadIdx.x; idx < rows * lp; idx += kTcThreads) Z[idx] = T[idx];
+  __syncthreads();
 }
 
-// Implicit CholeskyQR2 of Y = delta X from its Gram G = X^T M X (in G):
-// leaves RiY (l x l) in R such that Y RiY is orthonormal.  G, Ri, H are
-// clobbered.
-__device__ void orth2_implicit(float* G, float* R, float* Ri, float* H, int* keep, int l,
-                               int ld) {
-  chol(G, R, keep, l, ld);
-  tri_inv(R, keep, Ri, l, ld);                       // Ri1
-  mm(G, ld, false, Ri, ld, H, ld, l, l, l);          // H  = G Ri1
-  mm(Ri, ld, true, H, ld, G, ld, l, l, l);           // G2 = Ri1^T G Ri1
-  for (int idx = threadIdx.x; idx < l * l; idx += kTcThreads) H[(idx / l) * ld + idx % l] = Ri[(idx / l) * ld + idx % l];
-  __syncthreads();                                   // H = Ri1
-  chol(G, R, keep, l, ld);
-  tri_inv(R, keep, Ri, l, ld);                       // Ri2
-  mm(H, ld, false, Ri, ld, R, ld, l, l, l);          // RiY = Ri1 Ri2 (into R)
+// Implicit CholeskyQR of Y = delta X from its Gram G = X^T M X (in G, stride
+// ls).  passes = 1: Ri holds Ri1 (stride lp) with Y Ri1 orthonormal to
+// ~eps kappa^2.  passes = 2 (CholeskyQR2): R holds RiY = Ri1 Ri2 (stride
+// lp).  G, H, R, Ri are clobbered.
+__device__ void orth_implicit(float* G, float* R, float* Ri, float* H, int* keep, float* dinv,
+                              const uint16_t* pik, int l, int lp, int ls, int passes) {
+  chol(G, R, keep, dinv, pik, l, ls);
+  tri_inv(R, keep, Ri, l, ls, lp);                   // Ri1
+  if (passes < 2) return;
+  mm(G, ls, false, Ri, lp, H, ls, l, l, l);          // H  = G Ri1
+  mm(Ri, lp, true, H, ls, G, ls, l, l, l);           // G2 = Ri1^T G Ri1
+  for (int idx = threadIdx.x; idx < l * lp; idx += kTcThreads) H[idx] = Ri[idx];
+  __syncthreads();                                   // H = Ri1 (stride lp)
+  chol(G, R, keep, dinv, pik, l, ls);
+  tri_inv(R, keep, Ri, l, ls, lp);                   // Ri2
+  mm(H, lp, false, Ri, lp, R, lp, l, l, lp);         // RiY = Ri1 Ri2 (into R, stride lp)
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kTcThreads)
+__global__ void __launch_bounds__(kTcThreads, 2)
     build_tc_kernel(const TcBuildArgs a, const __grid_constant__ SegTable seg) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   const int d = a.d, l = a.l, r = a.r;
-  const int ld = (l & 1) ? l : l + 1;                 // odd row stride of the l x l matrices
-  const int rowsz = kDP * l;
-  const int region0 = max(2 * kDP * 128, ((3 * rowsz * 4) + 1023) & ~1023);
+  const int lp = (l + 3) & ~3;                        // padded sketch width (float4 rows)
+  const int ls = lp + 1;                              // odd row stride of l x l work matrices
+  const int rowsz = kDP * lp;
+  const int region0 = max(2 * kDP * 128, ((2 * rowsz * 4) + 1023) & ~1023);
   uint8_t* hi = sm;                                   // delta^T chunk, hi part (16 KB)
   uint8_t* lo = sm + kDP * 128;                       // lo part (16 KB)
   float* P1 = reinterpret_cast<float*>(sm);           // overlays hi/lo after phase A
   float* Z = P1 + rowsz;
-  float* Tb = Z + rowsz;
   float* X = reinterpret_cast<float*>(sm + region0);
   float* G = X + rowsz;
-  float* R = G + l * ld;
-  float* Ri = R + l * ld;
-  float* H = Ri + l * ld;
-  float* lam = H + l * ld;
+  float* R = G + lp * ls;
+  float* Ri = R + lp * ls;
+  float* H = Ri + lp * ls;
+  float* lam = H + lp * ls;
   float* cs = lam + kLmax;
   float* red = cs + 2 * kLmax;
   int* keep = reinterpret_cast<int*>(red + 32);
   int* pairs = keep + kLmax;
   int* order = pairs + 2 * kLmax;
+  float* dinv = reinterpret_cast<float*>(order + kLmax);
+  uint16_t* pik = reinterpret_cast<uint16_t*>(dinv + kLmax);   // upper-triangle (i, k) pairs
+  uint16_t* jitems = pik + kLmax * (kLmax + 1) / 2;               // Jacobi item table
   uint64_t* mbar = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(order + kLmax) + 7) & ~uintptr_t(7));
+      (reinterpret_cast<uintptr_t>(jitems + 3 * 32 * 32) + 7) & ~uintptr_t(7));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mbar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -367,9 +434,12 @@ __global__ void __launch_bounds__(kTcThreads)
     mbar_init(mbar, 1);
     fence_mbar_init();
     *abort_flag = 0;
+    int p = 0;
+    for (int i = 0; i < l; ++i)
+      for (int k = i; k < l; ++k) pik[p++] = static_cast<uint16_t>((i << 8) | k);
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc<kTmemCols>(tmem_slot);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -457,27 +527,27 @@ __global__ void __launch_bounds__(kTcThreads)
 
     // ---- phase B: subspace iteration on the feature side
     for (int idx = threadIdx.x; idx < rowsz; idx += kTcThreads) {
-      const int c = idx / l;
-      X[idx] = (c < d) ? __ldg(a.omega + idx) : 0.0f;
+      const int c = idx / lp, j = idx % lp;
+      X[idx] = (c < d && j < l) ? __ldg(a.omega + c * l + j) : 0.0f;
     }
     for (int it = 0; it < a.q; ++it) {
-      tmem_mx(tmem, X, P1, d, l);                     // P1 = M X
-      mm(X, l, true, P1, l, G, ld, l, kDP, l);        // G  = X^T M X = Y^T Y
-      orth2_implicit(G, R, Ri, H, keep, l, ld);       // R  = RiY
-      mm(P1, l, false, R, ld, Z, l, kDP, l, l);       // Z  = delta^T Q
-      orth2(Z, Tb, kDP, l, ld, G, R, Ri, keep);       // Z  = orth(Z)
+      tmem_mx(tmem, X, P1, d, lp);                        // P1 = M X = delta^T Y
+      mm(X, lp, true, P1, lp, G, ls, l, kDP, l);          // G  = X^T M X = Y^T Y
+      orth_implicit(G, R, Ri, H, keep, dinv, pik, l, lp, ls, 1);     // Ri: Y Ri orthonormal
+      mm(P1, lp, false, Ri, lp, Z, lp, kDP, l, lp);       // Z  = delta^T Q
+      orth1(Z, P1, kDP, l, lp, ls, G, R, Ri, keep, dinv, pik);       // Z  = orth(Z)
       for (int idx = threadIdx.x; idx < rowsz; idx += kTcThreads) X[idx] = Z[idx];
       __syncthreads();
     }
-    tmem_mx(tmem, X, P1, d, l);
-    mm(X, l, true, P1, l, G, ld, l, kDP, l);
-    orth2_implicit(G, R, Ri, H, keep, l, ld);         // R = RiY of the final Q
-    mm(P1, l, false, R, ld, Z, l, kDP, l, l);         // Z = B^T = delta^T Q
+    tmem_mx(tmem, X, P1, d, lp);
+    mm(X, lp, true, P1, lp, G, ls, l, kDP, l);
+    orth_implicit(G, R, Ri, H, keep, dinv, pik, l, lp, ls, 2);       // R = RiY (stride lp), CholeskyQR2
+    mm(P1, lp, false, R, lp, Z, lp, kDP, l, lp);          // Z = B^T = delta^T Q
 
     // ---- small SVD of B through B B^T = Z^T Z
-    mm(Z, l, true, Z, l, G, ld, l, kDP, l);
-    jacobi(G, H, l, ld, cs, reinterpret_cast<int*>(pairs), red);   // H = Ub
-    for (int i = threadIdx.x; i < l; i += kTcThreads) lam[i] = fmaxf(G[i * ld + i], 0.0f);
+    mm(Z, lp, true, Z, lp, G, ls, l, kDP, l);
+    jacobi(G, H, l, ls, cs, pairs, red, jitems);          // H = Ub (stride ls)
+    for (int i = threadIdx.x; i < l; i += kTcThreads) lam[i] = fmaxf(G[i * ls + i], 0.0f);
     __syncthreads();
     for (int i = threadIdx.x; i < l; i += kTcThreads) {
       int rank = 0;
@@ -511,21 +581,21 @@ __global__ void __launch_bounds__(kTcThreads)
         const float sj = sqrtf(lam[col]);
         if (sj > 1e-6f * sig_max && sj > 0.0f) {
           float acc = 0.0f;
-          for (int i = 0; i < l; ++i) acc = fmaf(Z[c * l + i], H[i * ld + col], acc);
+          for (int i = 0; i < l; ++i) acc = fmaf(Z[c * lp + i], H[i * ls + col], acc);
           v = acc / sj;
         }
       }
       store_out<T>(Wo + (static_cast<int64_t>(c) * a.A + slot) * r + j, v);
     }
     // ---- P = X RiY Ub_r diag(sigma_r)  (kDP x r, into P1)
-    mm(X, l, false, R, ld, Tb, l, kDP, l, l);
+    mm(X, lp, false, R, lp, Z, lp, kDP, l, lp);            // Z <- X RiY (B^T no longer needed)
     for (int idx = threadIdx.x; idx < kDP * r; idx += kTcThreads) {
       const int c = idx / r, j = idx % r;
       float v = 0.0f;
       if (j < l) {
         const int col = order[j];
         float acc = 0.0f;
-        for (int i = 0; i < l; ++i) acc = fmaf(Tb[c * l + i], H[i * ld + col], acc);
+        for (int i = 0; i < l; ++i) acc = fmaf(Z[c * lp + i], H[i * ls + col], acc);
         v = acc * sqrtf(lam[col]);
       }
       P1[c * r + j] = v;
@@ -533,23 +603,53 @@ __global__ void __launch_bounds__(kTcThreads)
     __syncthreads();
     // ---- U = delta P: rows of the segment, zero padding up to Tmax
     T* Uo = reinterpret_cast<T*>(a.U[kv]) + static_cast<int64_t>(unit) * a.Tmax * a.A * r;
+    constexpr int VEC = 16 / sizeof(T);                  // elements per 16-byte load
+    const bool vec_r = (r & 3) == 0;
     for (int t = threadIdx.x; t < a.Tmax; t += kTcThreads) {
       T* urow = Uo + (static_cast<int64_t>(t) * a.A + slot) * r;
-      float acc[kLmax];
+      float4 acc[kLmax / 4];
 #pragma unroll
-      for (int j = 0; j < kLmax; ++j) acc[j] = 0.0f;
+      for (int q4 = 0; q4 < kLmax / 4; ++q4) acc[q4] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       if (t < n) {
-        for (int c = 0; c < d; ++c) {
-          const float dv = to_f<T>(ex[t * es3 + c]) - to_f<T>(rf[t * rs3 + c]);
-          const float* pr = P1 + c * r;
+        for (int c0 = 0; c0 < d; c0 += VEC) {
+          const uint4 xe = *reinterpret_cast<const uint4*>(ex + t * es3 + c0);
+          const uint4 xr = *reinterpret_cast<const uint4*>(rf + t * rs3 + c0);
+          const T* pe = reinterpret_cast<const T*>(&xe);
+          const T* pq = reinterpret_cast<const T*>(&xr);
 #pragma unroll
-          for (int j = 0; j < kLmax; ++j)
-            if (j < r) acc[j] = fmaf(dv, pr[j], acc[j]);
+          for (int e = 0; e < VEC; ++e) {
+            const float dv = to_f<T>(pe[e]) - to_f<T>(pq[e]);
+            const float* pr = P1 + (c0 + e) * r;
+            if (vec_r) {
+#pragma unroll
+              for (int q4 = 0; q4 < kLmax / 4; ++q4) {
+                if (4 * q4 < r) {
+                  const float4 pv = *reinterpret_cast<const float4*>(pr + 4 * q4);
+                  acc[q4].x = fmaf(dv, pv.x, acc[q4].x);
+                  acc[q4].y = fmaf(dv, pv.y, acc[q4].y);
+                  acc[q4].z = fmaf(dv, pv.z, acc[q4].z);
+                  acc[q4].w = fmaf(dv, pv.w, acc[q4].w);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int q4 = 0; q4 < kLmax / 4; ++q4) {
+                float* av = reinterpret_cast<float*>(&acc[q4]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (4 * q4 + u < r) av[u] = fmaf(dv, pr[4 * q4 + u], av[u]);
+              }
+            }
+          }
         }
       }
 #pragma unroll
-      for (int j = 0; j < kLmax; ++j)
-        if (j < r) store_out<T>(urow + j, acc[j]);
+      for (int q4 = 0; q4 < kLmax / 4; ++q4) {
+        const float* av = reinterpret_cast<const float*>(&acc[q4]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (4 * q4 + u < r) store_out<T>(urow + 4 * q4 + u, av[u]);
+      }
     }
     // ---- pool insertion: the new anchor's summary is the held key mean
     if (a.summaries != nullptr && kv == 0) {
@@ -569,17 +669,33 @@ __global__ void __launch_bounds__(kTcThreads)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) tmem_dealloc<kTmemCols>(tmem);
 }
 
 size_t tc_build_smem(int l) {
-  const int ld = (l & 1) ? l : l + 1;
-  const int rowsz = kDP * l;
-  const int region0 = std::max(2 * kDP * 128, ((3 * rowsz * 4) + 1023) & ~1023);
-  size_t bytes = 1024 + static_cast<size_t>(region0) + static_cast<size_t>(rowsz) * 4 +
-                 static_cast<size_t>(4) * l * ld * 4 + (kLmax + 2 * kLmax + 32) * 4 +
-                 (kLmax + 2 * kLmax + kLmax) * 4 + 8 + 16 + 8;
-  return bytes;
+  const int lp = (l + 3) & ~3, ls = lp + 1;
+  const int rowsz = kDP * lp;
+  const int region0 = std::max(2 * kDP * 128, ((2 * rowsz * 4) + 1023) & ~1023);
+  return 1024 + static_cast<size_t>(region0) + static_cast<size_t>(rowsz) * 4 +
+         static_cast<size_t>(4) * lp * ls * 4 + (kLmax + 2 * kLmax + 32) * 4 +
+         (kLmax + 2 * kLmax + kLmax) * 4 + kLmax * 4 + (kLmax * (kLmax + 1) / 2) * 2 +
+         3 * 32 * 32 * 2 + 8 + 16 + 8;
+}
+
+// CTAs of this kernel that fit on one SM.  The occupancy API reports one CTA
+// per SM for every kernel that allocates TMEM, whatever it allocates; this
+// kernel takes kTmemCols of the 512 columns, so the bound comes from the
+// registers and the shared memory (and the launch bounds' two CTAs).
+cudaError_t resident_ctas(const void* fn, const DeviceInfo& di, size_t smem, int* out) {
+  cudaFuncAttributes fa{};
+  const cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+  if (e != cudaSuccess) return e;
+  const int regs = std::max(fa.numRegs, 1) * kTcThreads;
+  const int by_regs = di.regs_per_sm / regs;
+  const int by_smem = di.smem_per_sm / static_cast<int>(smem + 1024);
+  const int by_tmem = 512 / static_cast<int>(kTmemCols);
+  *out = std::max(1, std::min(std::min(by_regs, by_smem), std::min(by_tmem, 2)));
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -632,18 +748,31 @@ cudaError_t launch_build_tc(const Dims& dm, const SegTable& seg, kvc_dtype dtype
   if (mats > 0x7FFFFFFF) return cudaErrorInvalidValue;
   a.n_mats = static_cast<int32_t>(mats);
   const size_t smem = tc_build_smem(l);
-  const int per_sm = std::max(1, std::min(2, static_cast<int>(di.max_smem_optin / (smem + 1024))));
-  const int64_t slots = static_cast<int64_t>(di.sm_count) * per_sm;
-  const int grid = static_cast<int>(mats < slots ? mats : slots);
+  int per_sm = 1;
   if (dtype == KVC_BF16) {
     e = cudaFuncSetAttribute(build_tc_kernel<__nv_bfloat16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    // two CTAs per SM only fit with the largest shared-memory carveout
+    e = cudaFuncSetAttribute(build_tc_kernel<__nv_bfloat16>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    e = resident_ctas(reinterpret_cast<const void*>(build_tc_kernel<__nv_bfloat16>), di, smem, &per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = static_cast<int64_t>(di.sm_count) * std::max(per_sm, 1);
+    const int grid = static_cast<int>(mats < slots ? mats : slots);
     build_tc_kernel<__nv_bfloat16><<<grid, kTcThreads, smem, stream>>>(a, seg);
   } else {
     e = cudaFuncSetAttribute(build_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(build_tc_kernel<float>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    e = resident_ctas(reinterpret_cast<const void*>(build_tc_kernel<float>), di, smem, &per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = static_cast<int64_t>(di.sm_count) * std::max(per_sm, 1);
+    const int grid = static_cast<int>(mats < slots ? mats : slots);
     build_tc_kernel<float><<<grid, kTcThreads, smem, stream>>>(a, seg);
   }
   return cudaGetLastError();

@@ -221,6 +221,10 @@ cudaError_t device_info(DeviceInfo* out) {
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&di.regs_per_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+    if (e != cudaSuccess) return e;
     cache[dev] = di;
     have[dev] = true;
   }

@@ -47,7 +47,9 @@ kvc_status set_last_error(kvc_status st, const char* msg);
 // Device attributes cached per device by the host layer.
 struct DeviceInfo {
   int sm_count;
-  int max_smem_optin;
+  int max_smem_optin;      // per block
+  int smem_per_sm;         // per SM
+  int regs_per_sm;
 };
 cudaError_t device_info(DeviceInfo* out);
 

@@ -47,6 +47,8 @@ def _args():
     p.add_argument("--workload", default="llama2k")
     p.add_argument("--requests", type=int, default=0,
                    help="use only the first N requests of the workload (small profiling cases)")
+    p.add_argument("--segments", type=int, default=0,
+                   help="use only the first N PH segments (small profiling cases)")
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -423,6 +425,16 @@ def main():
         keep = [s for s in range(wl.S) if wl.seg_request[s] < args.requests]
         wl = dataclasses.replace(
             wl, R=args.requests, name="%s-r%d" % (wl.name, args.requests),
+            seg_request=tuple(wl.seg_request[s] for s in keep),
+            seg_start=tuple(wl.seg_start[s] for s in keep),
+            seg_len=tuple(wl.seg_len[s] for s in keep))
+    if 0 < args.segments < wl.S:
+        import dataclasses
+        keep = list(range(args.segments))
+        wl = dataclasses.replace(
+            wl, name="%s-s%d" % (wl.name, args.segments),
+            T=max(wl.seg_start[s] + wl.seg_len[s] for s in keep),
+            R=max(wl.seg_request[s] for s in keep) + 1,
             seg_request=tuple(wl.seg_request[s] for s in keep),
             seg_start=tuple(wl.seg_start[s] for s in keep),
             seg_len=tuple(wl.seg_len[s] for s in keep))
