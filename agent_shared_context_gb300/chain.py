@@ -6,7 +6,9 @@ workspaces) and drives the library: for edge j >= 1 it optionally builds the
 low-rank state of (exact_j - held_{j-1}) into the configured anchor slot
 (``kvc_build_states``) and then runs ``kvc_chain_edge`` with the held cache of
 agent j-1 as reference, so the corrected cache of agent j becomes the
-reference of edge j+1 (KVCMAS listing, Figure 1(c)).  Agent A0's cache is the
+reference of edge j+1 (KVCMAS listing, Figure 1(c)).  With ``fixed_ref``
+every edge corrects one fixed context-free reference instead (the
+non-chained variant of Figure 3 / Table 8).  Agent A0's cache is the
 exact one and is never written (edge 0 is a validated no-op).
 
 All arithmetic of the correction path runs in libkvc; this module only
@@ -46,13 +48,15 @@ def ph_row_mask(wl: Workload, device) -> torch.Tensor:
 class ChainRunner:
     def __init__(self, wl: Workload, inp: WorkloadInputs, device="cuda", use_dense: bool = True,
                  poison_ph: bool = False, stream: Optional[torch.cuda.Stream] = None,
-                 build: Optional[bool] = None):
+                 build: Optional[bool] = None, fixed_ref=None):
         self.wl = wl
         self.inp = inp
         self.device = torch.device(device)
         self.use_dense = use_dense
         self.stream = stream
         self.build = (wl.build_slot >= 0) if build is None else build
+        # non-chained variant: one fixed (context-free) reference for every edge
+        self.fixed_ref = fixed_ref
         self.seg = kvc.Segments.from_workload(wl)
         self.prm = kvc.params_from_workload(wl)
         S, L, H, A = wl.S, wl.L, wl.H, wl.A
@@ -93,7 +97,7 @@ class ChainRunner:
 
     def run_edge(self, j: int) -> None:
         wl, inp = self.wl, self.inp
-        refK, refV = self.held(j - 1)
+        refK, refV = self.held(j - 1) if self.fixed_ref is None else self.fixed_ref
         if j == 0:
             kvc.kvc_chain_edge(0, self.seg, self.prm, refK, refV, None, None, None, None, None,
                                None, None, None, None, None, None, None, None, None,

@@ -219,7 +219,7 @@ def segment_arrays(wl: Workload):
 # seeded generators
 # --------------------------------------------------------------------------
 _PURPOSE = {"base": 1, "pf": 2, "delta": 3, "anchor": 4, "summary": 5,
-            "omega": 6, "planted": 7, "visual": 8}
+            "omega": 6, "planted": 7, "visual": 8, "context_free": 9}
 
 
 def _generator(device: torch.device, wl: Workload, purpose: str, *key: int) -> torch.Generator:
@@ -280,6 +280,10 @@ class WorkloadInputs:
     edges: List[EdgeInputs]          # edge j (1-based) at index j-1
     omega: torch.Tensor              # [d, l] float32 test matrix for the builder
     planted_ratio: Tuple[float, float]
+    # context-free reference (the shared context prefilled without any agent
+    # prefix): E_0 minus A0's own planted delta on the PH rows
+    context_free_K: Optional[torch.Tensor] = None
+    context_free_V: Optional[torch.Tensor] = None
 
 
 def _seg_ratio(wl: Workload, planted: bool) -> float:
@@ -414,5 +418,31 @@ def generate(wl: Workload, device="cpu", edges: Optional[Sequence[int]] = None) 
 
     go = _generator(device, wl, "omega")
     omega = _randn((d, wl.l), go, device)
+    cfK, cfV = _context_free(wl, K0, V0, device)
     return WorkloadInputs(wl=wl, exact_K=exact_K, exact_V=exact_V, edges=edge_inputs,
-                          omega=omega, planted_ratio=(_seg_ratio(wl, False), _seg_ratio(wl, True)))
+                          omega=omega, planted_ratio=(_seg_ratio(wl, False), _seg_ratio(wl, True)),
+                          context_free_K=cfK, context_free_V=cfV)
+
+
+def _context_free(wl: Workload, K0: torch.Tensor, V0: torch.Tensor, device):
+    """E_cf = E_0 - Delta_0 on PH rows, Delta_0 drawn like an edge delta
+    (geometric spectrum at 0.4 tau of the cache norm, Haar factors, noise)."""
+    dt = wl.torch_dtype
+    cfK, cfV = K0.clone(), V0.clone()
+    for s in range(wl.S):
+        q, t0, n = wl.seg_request[s], wl.seg_start[s], wl.seg_len[s]
+        g = _generator(device, wl, "context_free", s)
+        for base, out in ((K0, cfK), (V0, cfV)):
+            rows = base[q, :, :, t0:t0 + n, :].float()
+            m = min(n, wl.d)
+            geo = wl.decay ** torch.arange(m, dtype=torch.float32, device=device)
+            rr = min(wl.r, m)
+            refn = torch.linalg.vector_norm(rows, dim=(-2, -1))
+            c = 0.4 * wl.tau * refn / torch.sqrt((geo[:rr] ** 2).sum())
+            sv = c.unsqueeze(-1) * geo
+            Uh = _haar(wl.L * wl.H, n, m, g, device).reshape(wl.L, wl.H, n, m)
+            Vh = _haar(wl.L * wl.H, wl.d, m, g, device).reshape(wl.L, wl.H, wl.d, m)
+            delta = torch.matmul(Uh * sv.unsqueeze(-2), Vh.transpose(-1, -2))
+            delta = delta + wl.noise * _randn((wl.L, wl.H, n, wl.d), g, device)
+            out[q, :, :, t0:t0 + n, :] = (rows - delta).to(dt)
+    return cfK, cfV

@@ -392,20 +392,27 @@ def chain_edge(edge: int, ref: Tuple[np.ndarray, np.ndarray], seg: Segments,
 def chain(exact_K: List[np.ndarray], exact_V: List[np.ndarray], seg: Segments,
           edge_states: List[States], edge_summaries: List[np.ndarray], top_k: int,
           temperature: float, tau: float, use_dense: bool = True,
-          build: Optional[dict] = None, reuse_ratio: Optional[float] = None):
+          build: Optional[dict] = None, reuse_ratio: Optional[float] = None,
+          fixed_ref: Optional[Tuple[np.ndarray, np.ndarray]] = None):
     """Run agents A0 -> A1 -> ... along the chain.
 
     held_0 = exact_0; for edge j >= 1 the reference is held_{j-1}.  When
     ``build`` = dict(slot, r, omega, q, frac) is given, slot ``slot`` of the
     edge's states is first rebuilt from (exact_j - held_{j-1}) (O2).  The
     output of edge j is held_j.  Returns the list of per-edge results (index
-    0 = A0 passthrough)."""
+    0 = A0 passthrough).
+
+    ``fixed_ref`` = (K, V) gives the non-chained variant (Figure 3, Table 8):
+    every edge corrects that one context-free reference instead of the held
+    cache of the previous agent (and builds its state against it)."""
     n_agents = len(exact_K)
     held = (np.asarray(exact_K[0], np.float64), np.asarray(exact_V[0], np.float64))
     results = [dict(out_K=held[0], out_V=held[1])]
     for j in range(1, n_agents):
         states = edge_states[j - 1].copy()
         extra = {}
+        if fixed_ref is not None:
+            held = (np.asarray(fixed_ref[0], np.float64), np.asarray(fixed_ref[1], np.float64))
         if build is not None:
             sigma, erank = build_states((exact_K[j], exact_V[j]), held, seg, build["r"],
                                         build["omega"], build["q"], build["slot"], states,

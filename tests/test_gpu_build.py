@@ -246,3 +246,44 @@ def test_pool_insert_matches_oracle(name):
             np.testing.assert_allclose(np64(summ[s]), osumm[s], rtol=0, atol=1e-5)
         else:
             assert torch.equal(summ[s], e.summaries[s])
+
+
+def test_non_chained_variant_matches_oracle():
+    """Non-chained variant (every edge corrects one context-free reference,
+    states built against it) on the GPU against O.chain(fixed_ref=...), and
+    the Figure 3(b) contrast measured on the GPU outputs."""
+    from agent_shared_context_gb300.chain import ChainRunner
+    gen = synth.scaled(synth.workload("longctx"), L=1, H=2, R=1, seg_len=[256, 200], A=1, r=8,
+                       top_k=1, fallback_frac=0.0, build_slot=0)
+    wl = dataclasses.replace(gen, tau=1e9)          # no fallback: compare corrections only
+    inp = synth.generate(gen, device="cuda")
+    orig = [dataclasses.replace(e, U_K=e.U_K.clone(), W_K=e.W_K.clone(), U_V=e.U_V.clone(),
+                                W_V=e.W_V.clone()) for e in inp.edges]
+    fixed = (inp.context_free_K, inp.context_free_V)
+    runner = ChainRunner(wl, inp, device="cuda", build=True, fixed_ref=fixed)
+    runner.run()
+    torch.cuda.synchronize()
+    assert int(runner.dev_status.item()) == 0
+    inp_o = dataclasses.replace(inp, edges=orig)
+    seg, EK, EV, st, sm = __import__("tests._harness", fromlist=["oracle_inputs"]).oracle_inputs(wl, inp_o)
+    b = dict(slot=0, r=wl.r, omega=np64(inp.omega), q=wl.power_iters)
+    res = O.chain(EK, EV, seg, st, sm, 1, wl.temperature, wl.tau, build=b,
+                  fixed_ref=(np64(fixed[0]), np64(fixed[1])))
+    for j in range(1, wl.edges + 1):
+        for key in ("out_K", "out_V"):
+            g = np64(getattr(runner.edges[j], key))
+            o = res[j][key]
+            for s in range(wl.S):
+                t0, n = wl.seg_start[s], wl.seg_len[s]
+                c = np.linalg.norm(o[0, :, :, t0:t0 + n] - np64(fixed[0 if key == "out_K" else 1])[0, :, :, t0:t0 + n])
+                err = np.linalg.norm(g[0, :, :, t0:t0 + n] - o[0, :, :, t0:t0 + n])
+                assert err <= 2e-2 * c + 2.0 ** -8 * np.linalg.norm(o[0, :, :, t0:t0 + n]), (j, key, s)
+    # contrast: chained errors below non-chained from agent 2 on (GPU outputs)
+    inp2 = synth.generate(gen, device="cuda")
+    chained = ChainRunner(wl, inp2, device="cuda", build=True)
+    chained.run()
+    torch.cuda.synchronize()
+    ec = [O.relative_error(np64(chained.edges[j].out_K), np64(inp2.exact_K[j])) for j in range(1, wl.edges + 1)]
+    ef = [O.relative_error(np64(runner.edges[j].out_K), np64(inp.exact_K[j])) for j in range(1, wl.edges + 1)]
+    print("M1 error per agent, chained:", ["%.3e" % x for x in ec], "non-chained:", ["%.3e" % x for x in ef])
+    assert all(c < f for c, f in zip(ec[1:], ef[1:]))

@@ -528,3 +528,36 @@ def test_pool_insert_fifo_and_exact_recovery():
         assert O.relative_error(out[0, :, :, t0:t0 + n], dense[kv][0, :, :, t0:t0 + n]) < 1e-12
     assert np.array_equal(summ[0], summ0[0])
     np.testing.assert_allclose(summ[1, 0, 1, slot], held[0][0, 0, 1, 20:35].mean(axis=0), atol=1e-15)
+
+
+# --------------------------------------------------------------------- NEXT-4
+def _m1_errors(res, EK):
+    return [O.relative_error(res[j]["out_K"], EK[j]) for j in range(len(EK))]
+
+
+def test_chained_beats_non_chained_reference():
+    """Listing Figure 3 / Table 8 (qualitative): correcting from the held
+    cache of the previous agent (chained) keeps the error of later agents
+    below correcting every agent from one context-free reference, whose
+    delta accumulates all agents' deviations.  Both with one built anchor
+    of rank 8 per segment."""
+    import dataclasses
+    from agent_shared_context_gb300 import synth
+    wl = synth.scaled(synth.workload("longctx"), L=1, H=2, R=1, seg_len=[128, 96], A=1, r=8,
+                      top_k=1, fallback_frac=0.0, build_slot=0)
+    inp = synth.generate(wl, device="cpu")
+    no_fallback = 1e9
+    seg = O.Segments(wl.seg_request, wl.seg_start, wl.seg_len)
+    EK = [t.double().numpy() for t in inp.exact_K]
+    EV = [t.double().numpy() for t in inp.exact_V]
+    st = [O.States(*(x.double().numpy() for x in (e.U_K, e.W_K, e.U_V, e.W_V))) for e in inp.edges]
+    sm = [e.summaries.double().numpy() for e in inp.edges]
+    build = dict(slot=0, r=wl.r, omega=inp.omega.double().numpy(), q=2)
+    chained = O.chain(EK, EV, seg, st, sm, 1, 0.1, no_fallback, build=build)
+    cf = (inp.context_free_K.double().numpy(), inp.context_free_V.double().numpy())
+    fixed = O.chain(EK, EV, seg, st, sm, 1, 0.1, no_fallback, build=build, fixed_ref=cf)
+    ec, ef = _m1_errors(chained, EK), _m1_errors(fixed, EK)
+    assert ec[0] == 0.0
+    for j in range(2, len(EK)):
+        assert ec[j] < ef[j], (j, ec, ef)
+    assert ef[-1] > ef[1]          # the non-chained error grows along the agents
