@@ -20,7 +20,7 @@ import torch
 import oracle as O
 from agent_shared_context_gb300 import synth
 
-from ._harness import check_out, np64, oracle_chain
+from ._harness import check_out, np64, oracle_chain, oracle_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -265,7 +265,7 @@ def test_non_chained_variant_matches_oracle():
     torch.cuda.synchronize()
     assert int(runner.dev_status.item()) == 0
     inp_o = dataclasses.replace(inp, edges=orig)
-    seg, EK, EV, st, sm = __import__("tests._harness", fromlist=["oracle_inputs"]).oracle_inputs(wl, inp_o)
+    seg, EK, EV, st, sm = oracle_inputs(wl, inp_o)
     b = dict(slot=0, r=wl.r, omega=np64(inp.omega), q=wl.power_iters)
     res = O.chain(EK, EV, seg, st, sm, 1, wl.temperature, wl.tau, build=b,
                   fixed_ref=(np64(fixed[0]), np64(fixed[1])))
