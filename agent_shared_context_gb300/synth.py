@@ -7,7 +7,9 @@ Shared Context in Multi-Agent Systems", thelatestinai listing of arXiv
 2609.34060: Figure 1 for the PF/PH trajectory structure, Table 3 for the
 per-workload thresholds tau, Table 4 for the ~9K-token vision-language
 trajectories).  It computes none of the method's outputs (no matching, no
-weights, no correction, no score, no factorisation of an observed delta).  Both
+weights, no correction, no score, no factorisation of an observed delta;
+the anchor representations of the rank mode use a library eigensolver on
+the generated keys, not the method's randomized factorisation).  Both
 the CUDA library's tests/benchmarks and the fp64 oracle consume the tensors it
 returns; neither side's arithmetic lives here.
 
@@ -37,6 +39,12 @@ Workloads (names used throughout the tests and the bench):
 * ``vl``        28 x 4 x 128, bf16, one 9,000-token trajectory (17 x 512 +
                 1 x 296 PH segments) whose keys in [1024, 7024) come from 64
                 Gaussian clusters (sigma 0.3), tau=0.6, 20% planted.
+* ``llama2k-rc32`` llama2k with rank-r_C anchor representations (r_C = 32,
+                listing Figure 13) in place of mean keys; base keys with a
+                geometric spectrum (decay 0.95 per singular value, effective
+                rank ~22, listing Figure 2).  Anchor representations are the
+                held keys' leading Gram eigenpairs (torch.linalg.eigh, an
+                input construction) plus a 10-50% Gaussian perturbation.
 
 ``scaled(workload, ...)`` shrinks a workload (layers, heads, requests, segment
 lengths) for oracle-sized parity cases while keeping its structure.
@@ -85,6 +93,9 @@ class Workload:
     anchor_perturb: float = 0.1
     build_slot: int = -1            # slot filled by the state builder (-1: none)
     visual: Optional[Tuple[int, int, int, float]] = None   # (start, stop, clusters, sigma)
+    summary_mode: str = "mean"      # anchor summaries: "mean" keys or "rank" r_C representations
+    rank_c: int = 32                # r_C of the representations ("rank" mode)
+    base_decay: Optional[float] = None   # geometric key spectrum of E_0 (None: i.i.d. keys)
     seed: int = 20260929
 
     @property
@@ -106,6 +117,10 @@ class Workload:
     @property
     def l(self) -> int:
         return self.r + self.oversample
+
+    @property
+    def l_c(self) -> int:
+        return self.rank_c + self.oversample
 
     @property
     def elem_bytes(self) -> int:
@@ -161,6 +176,12 @@ def _build_workloads() -> Dict[str, Workload]:
         seg_request=tuple([0] * 18), seg_start=st, seg_len=ln, n_agents=4,
         A=8, r=32, tau=0.6, fallback_frac=0.20,
         visual=(1024, 7024, 64, 0.3), seed=20260929 + 4)
+    req, st, ln = _uniform_segments(10, 1, 0, 2048)
+    w["llama2k-rc32"] = Workload(
+        name="llama2k-rc32", L=32, H=8, d=128, dtype="bf16", R=10, T=2048,
+        seg_request=req, seg_start=st, seg_len=ln, n_agents=4,
+        A=8, r=32, tau=0.32, fallback_frac=0.10, summary_mode="rank", rank_c=32,
+        base_decay=0.95, seed=20260929 + 5)
     return w
 
 
@@ -219,7 +240,8 @@ def segment_arrays(wl: Workload):
 # seeded generators
 # --------------------------------------------------------------------------
 _PURPOSE = {"base": 1, "pf": 2, "delta": 3, "anchor": 4, "summary": 5,
-            "omega": 6, "planted": 7, "visual": 8, "context_free": 9}
+            "omega": 6, "planted": 7, "visual": 8, "context_free": 9, "rep": 10,
+            "omega_c": 11}
 
 
 def _generator(device: torch.device, wl: Workload, purpose: str, *key: int) -> torch.Generator:
@@ -261,8 +283,9 @@ class EdgeInputs:
 
     U_*: [S, L, H, Tmax, A, r]  token factors (singular values folded in)
     W_*: [S, L, H, d, A, r]     feature factors
-    summaries: [S, L, H, A, d] float32 anchor summaries
+    summaries: [S, L, H, A, d] float32 anchor summaries (mean keys)
     planted: [S] bool, segments whose delta was scaled to exceed tau
+    reps: [S, L, H, A, d, r_C] float32 anchor representations ("rank" mode)
     """
     U_K: torch.Tensor
     W_K: torch.Tensor
@@ -270,6 +293,7 @@ class EdgeInputs:
     W_V: torch.Tensor
     summaries: torch.Tensor
     planted: torch.Tensor
+    reps: Optional[torch.Tensor] = None
 
 
 @dataclass
@@ -284,6 +308,7 @@ class WorkloadInputs:
     # prefix): E_0 minus A0's own planted delta on the PH rows
     context_free_K: Optional[torch.Tensor] = None
     context_free_V: Optional[torch.Tensor] = None
+    omega_c: Optional[torch.Tensor] = None   # [d, l_C] test matrix of the representations
 
 
 def _seg_ratio(wl: Workload, planted: bool) -> float:
@@ -315,6 +340,8 @@ def generate(wl: Workload, device="cpu", edges: Optional[Sequence[int]] = None) 
         g = _generator(device, wl, "base", q)
         kq = _randn((L, H, T, d), g, device)
         vq = _randn((L, H, T, d), g, device)
+        if wl.base_decay is not None:
+            kq = _spectral_keys(wl, T, g, device)
         if wl.visual is not None:
             lo, hi, ncl, sig = wl.visual
             gv = _generator(device, wl, "visual", q)
@@ -364,6 +391,9 @@ def generate(wl: Workload, device="cpu", edges: Optional[Sequence[int]] = None) 
             W_K = torch.zeros((S, L, H, d, A, r), dtype=dt, device=device)
             W_V = torch.zeros_like(W_K)
             summ = torch.zeros((S, L, H, A, d), dtype=torch.float32, device=device)
+            reps = None
+            if wl.summary_mode == "rank":
+                reps = torch.zeros((S, L, H, A, d, wl.rank_c), dtype=torch.float32, device=device)
         for s in range(S):
             q, t0, n = wl.seg_request[s], wl.seg_start[s], wl.seg_len[s]
             planted = bool(planted_masks[j - 1][s])
@@ -409,9 +439,12 @@ def generate(wl: Workload, device="cpu", edges: Optional[Sequence[int]] = None) 
                 gs = _generator(device, wl, "summary", j, s)
                 kmean = prevK[q, :, :, t0:t0 + n, :].float().mean(dim=2)      # [L, H, d]
                 summ[s] = kmean.unsqueeze(2) + wl.summary_noise * _randn((L, H, A, d), gs, device)
+                if reps is not None:
+                    reps[s] = _anchor_reps(wl, prevK[q, :, :, t0:t0 + n, :],
+                                           _generator(device, wl, "rep", j, s), device)
         if j in want:
             ein = EdgeInputs(U_K=U_K, W_K=W_K, U_V=U_V, W_V=W_V, summaries=summ,
-                             planted=planted_masks[j - 1].clone())
+                             planted=planted_masks[j - 1].clone(), reps=reps)
         edge_inputs.append(ein)
         exact_K.append(Kj)
         exact_V.append(Vj)
@@ -419,9 +452,54 @@ def generate(wl: Workload, device="cpu", edges: Optional[Sequence[int]] = None) 
     go = _generator(device, wl, "omega")
     omega = _randn((d, wl.l), go, device)
     cfK, cfV = _context_free(wl, K0, V0, device)
+    omega_c = None
+    if wl.summary_mode == "rank":
+        omega_c = _randn((d, wl.l_c), _generator(device, wl, "omega_c"), device)
     return WorkloadInputs(wl=wl, exact_K=exact_K, exact_V=exact_V, edges=edge_inputs,
                           omega=omega, planted_ratio=(_seg_ratio(wl, False), _seg_ratio(wl, True)),
-                          context_free_K=cfK, context_free_V=cfV)
+                          context_free_K=cfK, context_free_V=cfV, omega_c=omega_c)
+
+
+def _spectral_keys(wl: Workload, T: int, g: torch.Generator, device) -> torch.Tensor:
+    """[L, H, T, d] keys with singular values proportional to base_decay^i
+    (Haar singular vectors), scaled to unit mean square like N(0, 1) keys;
+    any segment's rows inherit the decaying spectrum."""
+    L, H, d = wl.L, wl.H, wl.d
+    m = min(T, d)
+    geo = wl.base_decay ** torch.arange(m, dtype=torch.float32, device=device)
+    sv = geo * math.sqrt(T * d / float((geo ** 2).sum()))
+    Uh = _haar(L * H, T, m, g, device).reshape(L, H, T, m)
+    Vh = _haar(L * H, d, m, g, device).reshape(L, H, d, m)
+    return torch.matmul(Uh * sv, Vh.transpose(-1, -2))
+
+
+def _anchor_reps(wl: Workload, keys: torch.Tensor, g: torch.Generator, device) -> torch.Tensor:
+    """[L, H, A, d, r_C] anchor representations for a segment whose held keys
+    are ``keys`` [L, H, n, d]: the truncated representation of those keys
+    (leading eigenpairs of the key Gram, float64) plus a Gaussian
+    perturbation whose relative Frobenius norm is drawn per anchor and unit
+    uniformly in [1, 5] x summary_noise, so anchors differ in similarity."""
+    L, H, d = wl.L, wl.H, wl.d
+    rc = wl.rank_c
+    k64 = keys.double()
+    gram = torch.matmul(k64.transpose(-1, -2), k64)
+    try:
+        lam, vec = torch.linalg.eigh(gram)
+    except RuntimeError:
+        # no device linear-algebra backend in this environment: factor on the host
+        lc, vc = torch.linalg.eigh(gram.cpu())
+        lam, vec = lc.to(gram.device), vc.to(gram.device)
+    lam = lam.flip(-1)[..., :rc].clamp_min(0.0)
+    vec = vec.flip(-1)[..., :rc]
+    rep = (vec * lam.sqrt().unsqueeze(-2)).float()                       # [L, H, d, rc]
+    rn = torch.linalg.vector_norm(rep, dim=(-2, -1), keepdim=True)
+    out = torch.empty((L, H, wl.A, d, rc), dtype=torch.float32, device=device)
+    for a in range(wl.A):
+        p = _randn((L, H, d, rc), g, device)
+        eps = wl.summary_noise * (1.0 + 4.0 * torch.rand((L, H, 1, 1), generator=g, device=device))
+        p = p * (eps * rn / torch.linalg.vector_norm(p, dim=(-2, -1), keepdim=True))
+        out[:, :, a] = rep + p
+    return out
 
 
 def _context_free(wl: Workload, K0: torch.Tensor, V0: torch.Tensor, device):

@@ -52,6 +52,17 @@ R9  randomized state: Y = delta Omega, HMT Algorithm 4.4 with q power
     |delta|_F^2 and returns l + 1 when they retain less than the fraction.
 R10 reuse-ratio mode: round(rho * S) segments are reused, the others (the
     largest scores, ties by lower index first) fall back.
+R12 rank-r_C cache representation (Figure 2: the base cache has a low
+    effective rank; Figure 13: ranks (r_C, r_Delta) = (32, 32), "Full" = the
+    uncompressed feature dimension): a segment's keys K [n, d] are
+    represented by Rep = W_C diag(sigma_C) [d, r_C], the r_C leading right
+    singular directions scaled by their singular values, from the same
+    randomized factorisation as R9 (test matrix Omega_C [d, r_C + p]).
+    Rep Rep^T is the rank-r_C approximation of the key Gram K^T K, so at
+    r_C = d it is K^T K itself.  The similarity of two representations is
+    the cosine of their Gram approximations, vec(Rq Rq^T) . vec(Ra Ra^T) /
+    (|Rq Rq^T|_F |Ra Ra^T|_F), 0 if either is zero; it replaces R4-R5 when
+    anchors carry representations instead of mean keys.
 
 Every function below is pinned by ``tests/test_oracle_pins.py`` against
 closed forms, special cases reducing to textbook routines, invariants, or
@@ -68,6 +79,7 @@ __all__ = [
     "eff_rank", "exact_state", "randomized_state", "build_unit", "build_states",
     "query_summary", "cosine", "select_and_weight", "match_anchors",
     "apply_correction", "segment_scores", "select_by_reuse_ratio", "pool_insert",
+    "cache_representation", "rep_similarity", "match_anchors_rep", "truncation_error_curve",
     "chain_edge", "chain",
     "relative_error", "Segments", "States",
 ]
@@ -284,6 +296,75 @@ def match_anchors(ref_K: np.ndarray, seg: Segments, summaries: np.ndarray,
 
 
 # ---------------------------------------------------------------------------
+# O3'-O4'  rank-r_C representation matching (reading R12; Figure 2, Figure 13)
+# ---------------------------------------------------------------------------
+def cache_representation(keys: np.ndarray, r_c: int, omega: np.ndarray,
+                         q: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Rep [d, r_C] = W_r diag(sigma_r) of the segment's keys [n, d] and the
+    l singular values of the sketch (reading R12).
+
+    The factorisation is the randomized one of the delta states (R9) applied
+    to the keys themselves; W holds the right singular vectors."""
+    _, W, sv = randomized_state(np.asarray(keys, np.float64), r_c, omega, q)
+    return W * sv[:r_c], sv
+
+
+def rep_similarity(rep_q: np.ndarray, rep_a: np.ndarray) -> float:
+    """Cosine of the two Gram approximations Rq Rq^T and Ra Ra^T (R12)."""
+    gq = np.asarray(rep_q, np.float64) @ np.asarray(rep_q, np.float64).T
+    ga = np.asarray(rep_a, np.float64) @ np.asarray(rep_a, np.float64).T
+    return cosine(gq.ravel(), ga.ravel())
+
+
+def match_anchors_rep(ref_K: np.ndarray, seg: Segments, anchor_reps: np.ndarray,
+                      top_k: int, temperature: float, r_c: int, omega_c: np.ndarray, q: int,
+                      frac: float = 0.9):
+    """Matching with rank-r_C representations (R12 in place of R4-R5).
+
+    anchor_reps [S, L, H, A, d, r_C].  Returns weights [S, L, H, A], best
+    [S, L, H], the query representations [S, L, H, d, r_C], the sketch
+    singular values [S, L, H, l_C] and the effective rank of the held keys
+    [S, L, H] (Figure 2's quantity, against |K|_F^2)."""
+    L, H, d = ref_K.shape[1], ref_K.shape[2], ref_K.shape[4]
+    A = anchor_reps.shape[3]
+    lc = omega_c.shape[1]
+    weights = np.zeros((seg.S, L, H, A))
+    best = np.zeros((seg.S, L, H), dtype=np.int64)
+    reps = np.zeros((seg.S, L, H, d, r_c))
+    sigma = np.zeros((seg.S, L, H, lc))
+    erank = np.zeros((seg.S, L, H), dtype=np.int64)
+    for s in range(seg.S):
+        req, t0, n = seg.request[s], seg.start[s], seg.length[s]
+        for layer in range(L):
+            for head in range(H):
+                keys = np.asarray(ref_K[req, layer, head, t0:t0 + n, :], np.float64)
+                rq, sv = cache_representation(keys, r_c, omega_c, q)
+                sims = [rep_similarity(rq, anchor_reps[s, layer, head, a]) for a in range(A)]
+                w, b = select_and_weight(sims, top_k, temperature)
+                weights[s, layer, head, :] = w
+                best[s, layer, head] = b
+                reps[s, layer, head] = rq
+                sigma[s, layer, head] = sv
+                erank[s, layer, head] = eff_rank(sv, frac, float(np.sum(keys * keys)))
+    return weights, best, reps, sigma, erank
+
+
+def truncation_error_curve(delta: np.ndarray, ranks: Sequence[int]) -> np.ndarray:
+    """Relative reconstruction error |delta - delta_k|_F / |delta|_F of the
+    best rank-k approximation for every k in ``ranks`` (Figure 7(b)).
+
+    By Eckart-Young it is sqrt(sum_{i >= k} sigma_i^2 / sum_i sigma_i^2),
+    evaluated from a full float64 SVD; 0 for a zero matrix."""
+    sv = np.linalg.svd(np.asarray(delta, np.float64), compute_uv=False)
+    e = sv * sv
+    total = float(np.sum(e))
+    out = np.zeros(len(ranks))
+    for i, k in enumerate(ranks):
+        out[i] = 0.0 if total == 0.0 else math.sqrt(max(float(np.sum(e[k:])), 0.0) / total)
+    return out
+
+
+# ---------------------------------------------------------------------------
 # O6-O7  correction and reliability (Figure 1(a)-(b) captions, Table 6)
 # ---------------------------------------------------------------------------
 def apply_correction(ref: Tuple[np.ndarray, np.ndarray], seg: Segments,
@@ -364,15 +445,22 @@ def chain_edge(edge: int, ref: Tuple[np.ndarray, np.ndarray], seg: Segments,
                summaries: np.ndarray, states: States, top_k: int,
                temperature: float, tau: float,
                dense: Optional[Tuple[np.ndarray, np.ndarray]],
-               out_init: Tuple[np.ndarray, np.ndarray], reuse_ratio: Optional[float] = None):
+               out_init: Tuple[np.ndarray, np.ndarray], reuse_ratio: Optional[float] = None,
+               rep: Optional[dict] = None):
     """One workflow edge.  Edge 0 returns ``ref`` unchanged (A0 is exact).
 
     For edge >= 1: match (O3-O5), correct (O6), score (O7); every flagged
     segment takes the ``dense`` rows when given.  ``out_init`` supplies the
-    rows outside the PH segments (the agent's own PF rows)."""
+    rows outside the PH segments (the agent's own PF rows).  With ``rep`` =
+    dict(r_c, omega, q) the anchors carry rank-r_C representations
+    (``summaries`` [S, L, H, A, d, r_C]) and the match follows R12."""
     if edge == 0:
         return dict(out_K=np.array(ref[0], np.float64), out_V=np.array(ref[1], np.float64))
-    weights, best, query = match_anchors(ref[0], seg, summaries, top_k, temperature)
+    if rep is None:
+        weights, best, query = match_anchors(ref[0], seg, summaries, top_k, temperature)
+    else:
+        weights, best, query, _, _ = match_anchors_rep(ref[0], seg, summaries, top_k, temperature,
+                                                       rep["r_c"], rep["omega"], rep["q"])
     cK, cV, partial = apply_correction(ref, seg, states, weights)
     score, fallback = segment_scores(partial, tau)
     if reuse_ratio is not None:
@@ -393,7 +481,8 @@ def chain(exact_K: List[np.ndarray], exact_V: List[np.ndarray], seg: Segments,
           edge_states: List[States], edge_summaries: List[np.ndarray], top_k: int,
           temperature: float, tau: float, use_dense: bool = True,
           build: Optional[dict] = None, reuse_ratio: Optional[float] = None,
-          fixed_ref: Optional[Tuple[np.ndarray, np.ndarray]] = None):
+          fixed_ref: Optional[Tuple[np.ndarray, np.ndarray]] = None,
+          rep: Optional[dict] = None):
     """Run agents A0 -> A1 -> ... along the chain.
 
     held_0 = exact_0; for edge j >= 1 the reference is held_{j-1}.  When
@@ -404,7 +493,11 @@ def chain(exact_K: List[np.ndarray], exact_V: List[np.ndarray], seg: Segments,
 
     ``fixed_ref`` = (K, V) gives the non-chained variant (Figure 3, Table 8):
     every edge corrects that one context-free reference instead of the held
-    cache of the previous agent (and builds its state against it)."""
+    cache of the previous agent (and builds its state against it).
+
+    ``rep`` = dict(r_c, omega, q) switches the match to rank-r_C
+    representations (reading R12); ``edge_summaries`` then holds the anchors'
+    representations."""
     n_agents = len(exact_K)
     held = (np.asarray(exact_K[0], np.float64), np.asarray(exact_V[0], np.float64))
     results = [dict(out_K=held[0], out_V=held[1])]
@@ -420,7 +513,7 @@ def chain(exact_K: List[np.ndarray], exact_V: List[np.ndarray], seg: Segments,
             extra = dict(sigma=sigma, eff_rank=erank, states=states)
         dense = (exact_K[j], exact_V[j]) if use_dense else None
         res = chain_edge(j, held, seg, edge_summaries[j - 1], states, top_k, temperature,
-                         tau, dense, (exact_K[j], exact_V[j]), reuse_ratio)
+                         tau, dense, (exact_K[j], exact_V[j]), reuse_ratio, rep)
         res.update(extra)
         results.append(res)
         held = (res["out_K"], res["out_V"])

@@ -561,3 +561,129 @@ def test_chained_beats_non_chained_reference():
     for j in range(2, len(EK)):
         assert ec[j] < ef[j], (j, ec, ef)
     assert ef[-1] > ef[1]          # the non-chained error grows along the agents
+
+
+# --------------------------------------------------------------------- NEXT-3
+def _orthonormal(rng, n, m):
+    q, rr = np.linalg.qr(rng.standard_normal((n, m)))
+    return q * np.sign(np.diag(rr))
+
+
+def _spectral(rng, n, d, sv):
+    """n x d matrix with singular values sv and Haar singular vectors."""
+    m = len(sv)
+    return (_orthonormal(rng, n, m) * np.asarray(sv)) @ _orthonormal(rng, d, m).T
+
+
+def test_rep_similarity_closed_form():
+    """Hand-worked: Rq = e1, Ra = [a e1, b e2]: Rq Rq^T = E11, Ra Ra^T =
+    diag(a^2, b^2, 0, ..), so the Gram cosine is a^2 / sqrt(a^4 + b^4)."""
+    d = 4
+    e = np.eye(d)
+    rq = e[:, :1]
+    for a, b in ((1.0, 1.0), (2.0, 1.0), (1.0, 3.0)):
+        ra = np.stack([a * e[:, 0], b * e[:, 1]], axis=1)
+        assert math.isclose(O.rep_similarity(rq, ra), a * a / math.sqrt(a ** 4 + b ** 4),
+                            rel_tol=1e-14)
+    # orthogonal column spaces and zero representations give 0
+    assert O.rep_similarity(e[:, :2], e[:, 2:]) == 0.0
+    assert O.rep_similarity(np.zeros((d, 2)), e[:, :2]) == 0.0
+
+
+def test_rep_similarity_invariants_and_trace_identity():
+    """Sign / rotation freedom of the factors does not change the similarity
+    (only Rep Rep^T enters); it is scale invariant, symmetric, in [0, 1], 1 on
+    itself, and equals |Rq^T Ra|_F^2 / (|Rq^T Rq|_F |Ra^T Ra|_F) (trace
+    identity <A A^T, B B^T> = |A^T B|_F^2)."""
+    rng = np.random.default_rng(31)
+    d, r = 16, 5
+    for _ in range(5):
+        rq = rng.standard_normal((d, r))
+        ra = rng.standard_normal((d, r + 2))
+        rot = _orthonormal(rng, r, r)
+        s = O.rep_similarity(rq, ra)
+        assert 0.0 <= s <= 1.0
+        assert math.isclose(O.rep_similarity(rq @ rot, ra), s, rel_tol=1e-12)
+        assert math.isclose(O.rep_similarity(-3.0 * rq, 0.5 * ra), s, rel_tol=1e-12)
+        assert math.isclose(O.rep_similarity(ra, rq), s, rel_tol=1e-12)
+        assert math.isclose(O.rep_similarity(rq, rq), 1.0, rel_tol=1e-12)
+        ident = np.sum((rq.T @ ra) ** 2) / (np.linalg.norm(rq.T @ rq) * np.linalg.norm(ra.T @ ra))
+        assert math.isclose(s, ident, rel_tol=1e-12)
+
+
+def test_cache_representation_exact_for_low_rank_and_full():
+    """Keys of rank <= r_C: Rep Rep^T is the key Gram K^T K exactly and the
+    sketch singular values are the keys' own (HMT: exact when rank <= l).
+    r_C = d ("Full" in Figure 13) reproduces K^T K for any keys."""
+    rng = np.random.default_rng(32)
+    n, d = 64, 16
+    sv = [5.0, 3.0, 2.0, 1.0, 0.5]
+    keys = _spectral(rng, n, d, sv)
+    om = rng.standard_normal((d, 8))
+    rep, sig = O.cache_representation(keys, 5, om, 2)
+    np.testing.assert_allclose(rep @ rep.T, keys.T @ keys, atol=1e-10)
+    np.testing.assert_allclose(sig[:5], sv, rtol=1e-10)
+    np.testing.assert_allclose(sig[5:], 0.0, atol=1e-10)
+    full = rng.standard_normal((n, d))
+    rep_f, _ = O.cache_representation(full, d, rng.standard_normal((d, d)), 1)
+    np.testing.assert_allclose(rep_f @ rep_f.T, full.T @ full, rtol=0, atol=1e-9)
+
+
+def test_cache_representation_matches_truncated_gram_on_decaying_spectrum():
+    """Geometric key spectrum: Rep Rep^T equals the best rank-r_C
+    approximation of K^T K computed by a symmetric eigensolver."""
+    rng = np.random.default_rng(33)
+    n, d, rc = 200, 32, 6
+    keys = _spectral(rng, n, d, [10.0 * 0.6 ** i for i in range(d)])
+    rep, _ = O.cache_representation(keys, rc, rng.standard_normal((d, rc + 8)), 2)
+    lam, vec = np.linalg.eigh(keys.T @ keys)
+    top = vec[:, ::-1][:, :rc] * lam[::-1][:rc]
+    best = top @ vec[:, ::-1][:, :rc].T
+    assert np.linalg.norm(rep @ rep.T - best) <= 1e-6 * np.linalg.norm(best)
+
+
+def test_match_anchors_rep_prefers_the_held_cache_representation():
+    """An anchor carrying the exact truncated representation of the held keys
+    wins (similarity ~1) against anchors of unrelated caches; the effective
+    rank reported for the held keys is that of their spectrum (Figure 2)."""
+    rng = np.random.default_rng(34)
+    n, d, rc, A = 96, 16, 4, 4
+    seg = O.Segments([0], [8], [n])
+    sv = [8.0, 4.0, 2.0, 1.0]
+    held = np.zeros((1, 1, 1, 8 + n + 4, d))
+    held[0, 0, 0, 8:8 + n] = _spectral(rng, n, d, sv)
+    keys = held[0, 0, 0, 8:8 + n]
+    u, s, vt = np.linalg.svd(keys, full_matrices=False)
+    exact_rep = vt[:rc].T * s[:rc]
+    reps = np.zeros((1, 1, 1, A, d, rc))
+    for a in range(A):
+        other = _spectral(rng, n, d, sv)
+        _, so, vo = np.linalg.svd(other, full_matrices=False)
+        reps[0, 0, 0, a] = vo[:rc].T * so[:rc]
+    reps[0, 0, 0, 2] = exact_rep
+    w, best, qrep, sig, er = O.match_anchors_rep(held, seg, reps, A, 0.1, rc,
+                                                 rng.standard_normal((d, rc + 4)), 2)
+    assert best[0, 0, 0] == 2
+    assert math.isclose(O.rep_similarity(qrep[0, 0, 0], exact_rep), 1.0, rel_tol=1e-10)
+    assert math.isclose(float(np.sum(w)), 1.0, rel_tol=1e-12)
+    assert np.argmax(w[0, 0, 0]) == 2
+    # energies 64, 16, 4, 1 of 85: 64 < 76.5 = 0.9 * 85 <= 64 + 16, so two
+    assert er[0, 0, 0] == 2
+
+
+def test_truncation_error_curve_geometric_closed_form():
+    """Figure 7(b): for singular values rho^i (i < m) the best rank-k error is
+    sqrt((rho^(2k) - rho^(2m)) / (1 - rho^(2m))); it agrees with the
+    Eckart-Young residual of the exact state (O2)."""
+    rng = np.random.default_rng(35)
+    n, d, m, rho = 80, 24, 16, 0.8
+    delta = _spectral(rng, n, d, [rho ** i for i in range(m)])
+    ks = [0, 1, 4, 8, 15, 16, 20]
+    got = O.truncation_error_curve(delta, ks)
+    for k, g in zip(ks, got):
+        kk = min(k, m)
+        want = math.sqrt((rho ** (2 * kk) - rho ** (2 * m)) / (1 - rho ** (2 * m)))
+        assert abs(g - want) < 1e-12
+    U, W, _ = O.exact_state(delta, 8)
+    assert math.isclose(O.relative_error(U @ W.T, delta), got[3], rel_tol=1e-10)
+    assert np.all(O.truncation_error_curve(np.zeros((4, 3)), [0, 1]) == 0.0)
