@@ -6,7 +6,8 @@ workspaces) and drives the library: for edge j >= 1 it optionally builds the
 low-rank state of (exact_j - held_{j-1}) into the configured anchor slot
 (``kvc_build_states``) and then runs ``kvc_chain_edge`` with the held cache of
 agent j-1 as reference, so the corrected cache of agent j becomes the
-reference of edge j+1 (KVCMAS listing, Figure 1(c)).  With ``fixed_ref``
+reference of edge j+1 (KVCMAS listing, Figure 1(c)).  Workloads in the
+rank-r_C summary mode pass the anchors' representations instead of mean keys.  With ``fixed_ref``
 every edge corrects one fixed context-free reference instead (the
 non-chained variant of Figure 3 / Table 8).  Agent A0's cache is the
 exact one and is never written (edge 0 is a validated no-op).
@@ -58,7 +59,10 @@ class ChainRunner:
         # non-chained variant: one fixed (context-free) reference for every edge
         self.fixed_ref = fixed_ref
         self.seg = kvc.Segments.from_workload(wl)
-        self.prm = kvc.params_from_workload(wl)
+        # rank-r_C mode: anchors carry representations and the params hold
+        # omega_c's address (inp keeps the tensor alive)
+        self.rank_mode = wl.summary_mode == "rank"
+        self.prm = kvc.params_from_workload(wl, omega_c=inp.omega_c if self.rank_mode else None)
         S, L, H, A = wl.S, wl.L, wl.H, wl.A
         dev = self.device
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -111,7 +115,8 @@ class ChainRunner:
                                  eo.eff_rank, self.build_ws, self.dev_status, stream=self.stream)
         dK = inp.exact_K[j] if self.use_dense else None
         dV = inp.exact_V[j] if self.use_dense else None
-        kvc.kvc_chain_edge(j, self.seg, self.prm, refK, refV, e.summaries, e.U_K, e.W_K, e.U_V,
+        summaries = e.reps if self.rank_mode else e.summaries
+        kvc.kvc_chain_edge(j, self.seg, self.prm, refK, refV, summaries, e.U_K, e.W_K, e.U_V,
                            e.W_V, dK, dV, eo.out_K, eo.out_V, eo.weights, eo.best, eo.score,
                            eo.fallback, self.workspace, self.dev_status, stream=self.stream)
 

@@ -34,6 +34,13 @@
 // One CTA per (segment, layer, KV head, K|V) matrix, persistent; the only
 // wait is on the MMA completion mbarrier, bounded by kWaitLimitNs.  Requires
 // d <= 128 and l <= 64 (the host falls back to the FP32 builder otherwise).
+//
+// Representation mode (rep != nullptr): the same iteration factors the keys
+// of one (segment, layer, head) themselves (no reference, no V half) and
+// writes Rep = B^T Ub_r = W_r diag(sigma_r) [d, r] -- the rank-r_C
+// representation of the keys (listing, Figure 2 and Figure 13) -- instead of
+// U and W.  bf16 keys are exact in bf16, so the lo parts vanish and only the
+// hi x hi MMA is issued.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -60,6 +67,7 @@ struct TcBuildArgs {
   int64_t es[2][4];
   int64_t rs[2][4];
   const float* omega;        // [d, l]
+  float* rep;                // representation mode: [units, d, r] (else nullptr)
   char* U[2];
   char* W[2];
   float* sigma;
@@ -449,9 +457,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint32_t mph = 0;
   bool committed = false;
 
+  const bool rep_mode = a.rep != nullptr;
+  // the difference of two bf16 caches needs hi + lo; bf16 keys alone are exact in hi
+  const bool need_lo = !(rep_mode && sizeof(T) == 2);
   for (int mat = blockIdx.x; mat < a.n_mats; mat += gridDim.x) {
-    const int kv = mat & 1;
-    const int unit = mat >> 1;
+    const int kv = rep_mode ? 0 : (mat & 1);
+    const int unit = rep_mode ? mat : (mat >> 1);
     const int h = unit % a.H;
     const int lyr = (unit / a.H) % a.L;
     const int s = unit / (a.H * a.L);
@@ -461,9 +472,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     const T* ex = reinterpret_cast<const T*>(a.exact[kv]) + seg.req[s] * a.es[kv][0] +
                   lyr * a.es[kv][1] + h * a.es[kv][2] +
                   static_cast<int64_t>(seg.start[s]) * a.es[kv][3];
-    const T* rf = reinterpret_cast<const T*>(a.ref[kv]) + seg.req[s] * a.rs[kv][0] +
-                  lyr * a.rs[kv][1] + h * a.rs[kv][2] +
-                  static_cast<int64_t>(seg.start[s]) * a.rs[kv][3];
+    const T* rf = rep_mode ? nullptr
+                           : reinterpret_cast<const T*>(a.ref[kv]) + seg.req[s] * a.rs[kv][0] +
+                                 lyr * a.rs[kv][1] + h * a.rs[kv][2] +
+                                 static_cast<int64_t>(seg.start[s]) * a.rs[kv][3];
     const int64_t es3 = a.es[kv][3], rs3 = a.rs[kv][3];
 
     // ---- phase A: M = delta^T delta on tcgen05 from split-bf16 chunks
@@ -482,7 +494,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           for (int e1 = 0; e1 < 2; ++e1) {
             const int t = t0 + 2 * e2 + e1;
             float v = 0.0f;
-            if (c < d && t < n) v = to_f<T>(ex[t * es3 + c]) - to_f<T>(rf[t * rs3 + c]);
+            if (c < d && t < n)
+              v = to_f<T>(ex[t * es3 + c]) - (rf != nullptr ? to_f<T>(rf[t * rs3 + c]) : 0.0f);
             dv[e1] = v;
             ss = fmaf(v, v, ss);
           }
@@ -506,9 +519,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           const uint64_t dh = desc_kmajor_sw128(hb + ks * 32);
           const uint64_t dl = desc_kmajor_sw128(lb + ks * 32);
           mma_bf16_ss(tmem, dh, dh, kIdescM, (kc | ks) != 0 ? 1u : 0u);
-          mma_bf16_ss(tmem, dh, dl, kIdescM, 1u);
-          mma_bf16_ss(tmem, dl, dh, kIdescM, 1u);
-          mma_bf16_ss(tmem, dl, dl, kIdescM, 1u);
+          if (need_lo) {
+            mma_bf16_ss(tmem, dh, dl, kIdescM, 1u);
+            mma_bf16_ss(tmem, dl, dh, kIdescM, 1u);
+            mma_bf16_ss(tmem, dl, dl, kIdescM, 1u);
+          }
         }
         mma_commit(mbar);
         committed = true;
@@ -556,20 +571,37 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      float* sg = a.sigma + (static_cast<int64_t>(unit) * 2 + kv) * l;
+      const int64_t mi = rep_mode ? static_cast<int64_t>(unit) : static_cast<int64_t>(unit) * 2 + kv;
+      float* sg = a.sigma != nullptr ? a.sigma + mi * l : nullptr;
       float cum = 0.0f;
       int er = l + 1;
       const float target = a.energy_frac * total;
       for (int k = 0; k < l; ++k) {
         const float lk = lam[order[k]];
-        sg[k] = sqrtf(lk);
+        if (sg != nullptr) sg[k] = sqrtf(lk);
         cum += lk;
         if (er == l + 1 && cum >= target) er = k + 1;
       }
       if (!(total > 0.0f)) er = 0;
-      a.eff_rank[static_cast<int64_t>(unit) * 2 + kv] = er;
+      if (a.eff_rank != nullptr) a.eff_rank[mi] = er;
     }
     const float sig_max = sqrtf(lam[order[0]]);
+
+    if (rep_mode) {
+      // ---- Rep = B^T Ub_r (= W_r diag(sigma_r)), [d, r] fp32
+      float* ro = a.rep + static_cast<int64_t>(unit) * d * r;
+      for (int idx = threadIdx.x; idx < d * r; idx += kTcThreads) {
+        const int c = idx / r, j = idx % r;
+        float acc = 0.0f;
+        if (j < l) {
+          const int col = order[j];
+          for (int i = 0; i < l; ++i) acc = fmaf(Z[c * lp + i], H[i * ls + col], acc);
+        }
+        ro[idx] = acc;
+      }
+      __syncthreads();
+      continue;
+    }
 
     // ---- W = B^T Ub_r diag(1 / sigma_r)
     T* Wo = reinterpret_cast<T*>(a.W[kv]) + static_cast<int64_t>(unit) * d * a.A * r;
@@ -702,15 +734,44 @@ cudaError_t resident_ctas(const void* fn, const DeviceInfo& di, size_t smem, int
 
 bool build_tc_supported(const Dims& dm, int l) { return dm.d <= kDP && l <= kLmax && dm.r <= kLmax; }
 
+namespace {
+
+cudaError_t launch_tc(TcBuildArgs& a, kvc_dtype dtype, const SegTable& seg, int64_t mats,
+                      cudaStream_t stream) {
+  DeviceInfo di{};
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  if (mats <= 0) return cudaSuccess;
+  if (mats > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  a.n_mats = static_cast<int32_t>(mats);
+  const size_t smem = tc_build_smem(a.l);
+  const void* fn = dtype == KVC_BF16 ? reinterpret_cast<const void*>(build_tc_kernel<__nv_bfloat16>)
+                                     : reinterpret_cast<const void*>(build_tc_kernel<float>);
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  // two CTAs per SM only fit with the largest shared-memory carveout
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
+  int per_sm = 1;
+  e = resident_ctas(fn, di, smem, &per_sm);
+  if (e != cudaSuccess) return e;
+  const int64_t slots = static_cast<int64_t>(di.sm_count) * std::max(per_sm, 1);
+  const int grid = static_cast<int>(mats < slots ? mats : slots);
+  if (dtype == KVC_BF16)
+    build_tc_kernel<__nv_bfloat16><<<grid, kTcThreads, smem, stream>>>(a, seg);
+  else
+    build_tc_kernel<float><<<grid, kTcThreads, smem, stream>>>(a, seg);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_build_tc(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
                             const View exactv[2], const View refv[2], const float* omega, int l,
                             int q, float energy_frac, int slot, void* U[2], void* W[2],
                             float* sigma, int32_t* eff_rank, int32_t* dev_status,
                             cudaStream_t stream, const uint8_t* seg_mask, const int32_t* seg_slot,
                             float* summaries) {
-  DeviceInfo di{};
-  cudaError_t e = device_info(&di);
-  if (e != cudaSuccess) return e;
   TcBuildArgs a{};
   for (int kv = 0; kv < 2; ++kv) {
     a.exact[kv] = static_cast<const char*>(exactv[kv].base);
@@ -727,6 +788,7 @@ cudaError_t launch_build_tc(const Dims& dm, const SegTable& seg, kvc_dtype dtype
     a.W[kv] = static_cast<char*>(W[kv]);
   }
   a.omega = omega;
+  a.rep = nullptr;
   a.sigma = sigma;
   a.eff_rank = eff_rank;
   a.dev_status = dev_status;
@@ -743,39 +805,34 @@ cudaError_t launch_build_tc(const Dims& dm, const SegTable& seg, kvc_dtype dtype
   a.seg_mask = seg_mask;
   a.seg_slot = seg_slot;
   a.summaries = summaries;
-  const int64_t mats = dm.units() * 2;
-  if (mats <= 0) return cudaSuccess;
-  if (mats > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  a.n_mats = static_cast<int32_t>(mats);
-  const size_t smem = tc_build_smem(l);
-  int per_sm = 1;
-  if (dtype == KVC_BF16) {
-    e = cudaFuncSetAttribute(build_tc_kernel<__nv_bfloat16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    // two CTAs per SM only fit with the largest shared-memory carveout
-    e = cudaFuncSetAttribute(build_tc_kernel<__nv_bfloat16>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    e = resident_ctas(reinterpret_cast<const void*>(build_tc_kernel<__nv_bfloat16>), di, smem, &per_sm);
-    if (e != cudaSuccess) return e;
-    const int64_t slots = static_cast<int64_t>(di.sm_count) * std::max(per_sm, 1);
-    const int grid = static_cast<int>(mats < slots ? mats : slots);
-    build_tc_kernel<__nv_bfloat16><<<grid, kTcThreads, smem, stream>>>(a, seg);
-  } else {
-    e = cudaFuncSetAttribute(build_tc_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(build_tc_kernel<float>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    e = resident_ctas(reinterpret_cast<const void*>(build_tc_kernel<float>), di, smem, &per_sm);
-    if (e != cudaSuccess) return e;
-    const int64_t slots = static_cast<int64_t>(di.sm_count) * std::max(per_sm, 1);
-    const int grid = static_cast<int>(mats < slots ? mats : slots);
-    build_tc_kernel<float><<<grid, kTcThreads, smem, stream>>>(a, seg);
-  }
-  return cudaGetLastError();
+  return launch_tc(a, dtype, seg, dm.units() * 2, stream);
+}
+
+cudaError_t launch_build_rep(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
+                             const View& keys, const float* omega_c, int l_c, int r_c, int q,
+                             float energy_frac, float* rep, float* sigma, int32_t* eff_rank,
+                             int32_t* dev_status, cudaStream_t stream) {
+  TcBuildArgs a{};
+  a.exact[0] = static_cast<const char*>(keys.base);
+  a.es[0][0] = keys.s_req;
+  a.es[0][1] = keys.s_layer;
+  a.es[0][2] = keys.s_head;
+  a.es[0][3] = keys.s_tok;
+  a.omega = omega_c;
+  a.rep = rep;
+  a.sigma = sigma;
+  a.eff_rank = eff_rank;
+  a.dev_status = dev_status;
+  a.L = dm.L;
+  a.H = dm.H;
+  a.d = dm.d;
+  a.Tmax = dm.Tmax;
+  a.A = 1;
+  a.r = r_c;
+  a.l = l_c;
+  a.q = q;
+  a.energy_frac = energy_frac;
+  return launch_tc(a, dtype, seg, dm.units(), stream);
 }
 
 }  // namespace kvc

@@ -31,9 +31,17 @@ kvc_status cuda_fail(cudaError_t e, const char* what) {
   return fail(KVC_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+#define KVC_TRY(expr)                    \
+  do {                                   \
+    const kvc_status _st = (expr);       \
+    if (_st != KVC_OK) return _st;       \
+  } while (0)
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t elem_bytes(kvc_dtype t) { return t == KVC_BF16 ? 2 : 4; }
+
+size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
 // ------------------------------------------------------------ descriptors
 kvc_status check_segments(const kvc_segments* seg, SegTable* tab) {
@@ -83,6 +91,8 @@ kvc_status check_segments(const kvc_segments* seg, SegTable* tab) {
   return KVC_OK;
 }
 
+kvc_status check_rep_params(const kvc_segments* seg, const kvc_params* prm);
+
 kvc_status check_params(const kvc_segments* seg, const kvc_params* prm, bool need_rank,
                         bool need_match, bool need_build) {
   if (prm == nullptr) return fail(KVC_ERR_INVALID_ARGUMENT, "params descriptor is NULL");
@@ -99,6 +109,10 @@ kvc_status check_params(const kvc_segments* seg, const kvc_params* prm, bool nee
       return fail(KVC_ERR_INVALID_ARGUMENT, "top_k = %d outside [1, %d]", prm->top_k, A);
     if (!(prm->temperature > 0.0f) || !std::isfinite(prm->temperature))
       return fail(KVC_ERR_INVALID_ARGUMENT, "temperature must be finite and > 0");
+    if (prm->summary_mode != 0 && prm->summary_mode != 1)
+      return fail(KVC_ERR_INVALID_ARGUMENT, "summary_mode = %d is neither 0 nor 1",
+                  prm->summary_mode);
+    if (prm->summary_mode == 1) KVC_TRY(check_rep_params(seg, prm));
   }
   if (need_rank) {
     if (!(prm->tau >= 0.0f)) return fail(KVC_ERR_INVALID_ARGUMENT, "tau must be >= 0 (not NaN)");
@@ -122,6 +136,29 @@ kvc_status check_params(const kvc_segments* seg, const kvc_params* prm, bool nee
         return fail(KVC_ERR_SHAPE, "segment %d: length %d < rank + oversample = %d", s,
                     seg->seg_len[s], l);
   }
+  return KVC_OK;
+}
+
+// Parameters of the rank-r_C representations (summary_mode 1).
+kvc_status check_rep_params(const kvc_segments* seg, const kvc_params* prm) {
+  const int rc = prm->rank_c;
+  if (rc < 1 || rc > 64) return fail(KVC_ERR_INVALID_ARGUMENT, "rank_c = %d outside [1, 64]", rc);
+  if (prm->oversample < 0) return fail(KVC_ERR_INVALID_ARGUMENT, "oversample < 0");
+  const int lc = rc + prm->oversample;
+  if (lc > std::min(seg->d, 64))
+    return fail(KVC_ERR_UNSUPPORTED, "rank_c + oversample = %d exceeds min(d, 64)", lc);
+  if (seg->d > 128)
+    return fail(KVC_ERR_UNSUPPORTED, "representations need d <= 128 (got %d)", seg->d);
+  if (prm->power_iters < 0 || prm->power_iters > 8)
+    return fail(KVC_ERR_INVALID_ARGUMENT, "power_iters = %d outside [0, 8]", prm->power_iters);
+  if (!(prm->energy_frac > 0.0f && prm->energy_frac <= 1.0f))
+    return fail(KVC_ERR_INVALID_ARGUMENT, "energy_frac must be in (0, 1]");
+  if (prm->omega_c == nullptr)
+    return fail(KVC_ERR_INVALID_ARGUMENT, "omega_c is NULL (summary_mode 1)");
+  for (int s = 0; s < seg->S; ++s)
+    if (seg->seg_len[s] < lc)
+      return fail(KVC_ERR_SHAPE, "segment %d: length %d < rank_c + oversample = %d", s,
+                  seg->seg_len[s], lc);
   return KVC_OK;
 }
 
@@ -172,12 +209,6 @@ Dims make_dims(const kvc_segments* seg, const kvc_params* prm) {
   d.r = prm ? prm->rank : 0;
   return d;
 }
-
-#define KVC_TRY(expr)                    \
-  do {                                   \
-    const kvc_status _st = (expr);       \
-    if (_st != KVC_OK) return _st;       \
-  } while (0)
 
 // Shared validation of the correction inputs/outputs.
 kvc_status check_apply_args(const kvc_segments* seg, const kvc_cache_view& ref_K,
@@ -394,6 +425,10 @@ kvc_status kvc_match_anchors(const kvc_segments* seg, const kvc_params* prm, kvc
   static thread_local SegTable tab;
   KVC_TRY(check_segments(seg, &tab));
   KVC_TRY(check_params(seg, prm, false, true, false));
+  if (prm->summary_mode != 0)
+    return fail(KVC_ERR_INVALID_ARGUMENT,
+                "kvc_match_anchors matches mean keys (summary_mode 0); use "
+                "kvc_match_representation for summary_mode 1");
   KVC_TRY(check_view(seg, ref_K, "ref_K"));
   KVC_TRY(check_dev_ptr(summaries, "summaries"));
   KVC_TRY(check_dev_ptr(weights, "weights"));
@@ -404,6 +439,52 @@ kvc_status kvc_match_anchors(const kvc_segments* seg, const kvc_params* prm, kvc
   const cudaError_t e = launch_match(dm, tab, seg->dtype, to_view(ref_K), summaries, prm->top_k,
                                      prm->temperature, weights, best, query, dev_status, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kvc_match_anchors launch");
+  return KVC_OK;
+}
+
+// --------------------------------------------------------------- representations
+kvc_status kvc_build_representation(const kvc_segments* seg, const kvc_params* prm,
+                                    kvc_cache_view cache_K, float* rep, float* rep_sigma,
+                                    int32_t* rep_eff_rank, int32_t* dev_status,
+                                    cudaStream_t stream) {
+  static thread_local SegTable tab;
+  KVC_TRY(check_segments(seg, &tab));
+  if (prm == nullptr) return fail(KVC_ERR_INVALID_ARGUMENT, "params descriptor is NULL");
+  if (prm->summary_mode != 1)
+    return fail(KVC_ERR_INVALID_ARGUMENT, "kvc_build_representation needs summary_mode 1");
+  KVC_TRY(check_rep_params(seg, prm));
+  KVC_TRY(check_view(seg, cache_K, "cache_K"));
+  KVC_TRY(check_dev_ptr(rep, "rep", true));
+  KVC_TRY(check_dev_ptr(dev_status, "dev_status"));
+  if (seg->S == 0) return KVC_OK;
+  const Dims dm = make_dims(seg, prm);
+  const cudaError_t e = launch_build_rep(dm, tab, seg->dtype, to_view(cache_K), prm->omega_c,
+                                         prm->rank_c + prm->oversample, prm->rank_c,
+                                         prm->power_iters, prm->energy_frac, rep, rep_sigma,
+                                         rep_eff_rank, dev_status, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_build_representation launch");
+  return KVC_OK;
+}
+
+kvc_status kvc_match_representation(const kvc_segments* seg, const kvc_params* prm,
+                                    const float* query_rep, const float* anchor_reps,
+                                    float* weights, int32_t* best, int32_t* dev_status,
+                                    cudaStream_t stream) {
+  static thread_local SegTable tab;
+  KVC_TRY(check_segments(seg, &tab));
+  KVC_TRY(check_params(seg, prm, false, true, false));
+  if (prm->summary_mode != 1)
+    return fail(KVC_ERR_INVALID_ARGUMENT, "kvc_match_representation needs summary_mode 1");
+  KVC_TRY(check_dev_ptr(query_rep, "query_rep", true));
+  KVC_TRY(check_dev_ptr(anchor_reps, "anchor_reps", true));
+  KVC_TRY(check_dev_ptr(weights, "weights"));
+  KVC_TRY(check_dev_ptr(best, "best"));
+  KVC_TRY(check_dev_ptr(dev_status, "dev_status"));
+  if (seg->S == 0) return KVC_OK;
+  const Dims dm = make_dims(seg, prm);
+  const cudaError_t e = launch_match_rep(dm, query_rep, anchor_reps, prm->rank_c, prm->top_k,
+                                         prm->temperature, weights, best, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kvc_match_representation launch");
   return KVC_OK;
 }
 
@@ -458,10 +539,12 @@ kvc_status kvc_apply_correction(const kvc_segments* seg, const kvc_params* prm,
 
 // --------------------------------------------------------------- chain
 size_t kvc_chain_edge_workspace(const kvc_segments* seg, const kvc_params* prm) {
-  (void)prm;
   if (seg == nullptr || seg->S <= 0) return 0;
-  const size_t bytes = static_cast<size_t>(seg->S) * seg->L * seg->H * 4 * sizeof(float);
-  return (bytes + 255) & ~static_cast<size_t>(255);
+  const size_t units = static_cast<size_t>(seg->S) * seg->L * seg->H;
+  size_t bytes = round256(units * 4 * sizeof(float));          // per-unit norms
+  if (prm != nullptr && prm->summary_mode == 1 && prm->rank_c > 0 && seg->d > 0)
+    bytes += round256(units * seg->d * prm->rank_c * sizeof(float));   // query representations
+  return bytes;
 }
 
 kvc_status kvc_chain_edge(int32_t edge, const kvc_segments* seg, const kvc_params* prm,
@@ -508,8 +591,22 @@ kvc_status kvc_chain_edge(int32_t edge, const kvc_segments* seg, const kvc_param
   if (seg->S == 0) return KVC_OK;
   const Dims dm = make_dims(seg, prm);
   float* partial = static_cast<float*>(workspace);
-  cudaError_t e = launch_match(dm, tab, seg->dtype, to_view(ref_K), summaries, prm->top_k,
-                               prm->temperature, weights, best, nullptr, dev_status, stream);
+  cudaError_t e;
+  if (prm->summary_mode == 1) {
+    if (!aligned16(summaries))
+      return fail(KVC_ERR_ALIGNMENT, "summaries (anchor representations) must be 16-byte aligned");
+    float* qrep = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                           round256(static_cast<size_t>(dm.units()) * 4 * sizeof(float)));
+    e = launch_build_rep(dm, tab, seg->dtype, to_view(ref_K), prm->omega_c,
+                         prm->rank_c + prm->oversample, prm->rank_c, prm->power_iters,
+                         prm->energy_frac, qrep, nullptr, nullptr, dev_status, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvc_chain_edge representation launch");
+    e = launch_match_rep(dm, qrep, summaries, prm->rank_c, prm->top_k, prm->temperature, weights,
+                         best, stream);
+  } else {
+    e = launch_match(dm, tab, seg->dtype, to_view(ref_K), summaries, prm->top_k,
+                     prm->temperature, weights, best, nullptr, dev_status, stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "kvc_chain_edge match launch");
   KVC_TRY(apply_impl(seg, prm, tab, ref_K, ref_V, U_K, W_K, U_V, W_V, weights, out_K, out_V,
                      partial, score, fallback, dev_status, stream));

@@ -107,6 +107,20 @@ cudaError_t launch_build_tc(const Dims& dm, const SegTable& seg, kvc_dtype dtype
                             cudaStream_t stream, const uint8_t* seg_mask, const int32_t* seg_slot,
                             float* summaries);
 
+// Rank-r_C representations of the keys of every (segment, layer, head) on
+// the tcgen05 builder (d <= 128, l_c <= 64): rep [units, d, r_c] fp32;
+// sigma [units, l_c] and eff_rank [units] may be nullptr.
+cudaError_t launch_build_rep(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
+                             const View& keys, const float* omega_c, int l_c, int r_c, int q,
+                             float energy_frac, float* rep, float* sigma, int32_t* eff_rank,
+                             int32_t* dev_status, cudaStream_t stream);
+
+// Gram-cosine similarities of query and anchor representations, top-k
+// softmax weights and argmax.
+cudaError_t launch_match_rep(const Dims& dm, const float* query_rep, const float* anchor_reps,
+                             int r_c, int top_k, float temperature, float* weights, int32_t* best,
+                             cudaStream_t stream);
+
 // Anchor pool: pool_next[s] += 1 for every flagged segment.
 cudaError_t launch_pool_advance(const Dims& dm, const uint8_t* fallback, int32_t* pool_next,
                                 cudaStream_t stream);

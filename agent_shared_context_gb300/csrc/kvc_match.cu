@@ -8,6 +8,12 @@
 // the top_k set ordered by (-sim, index), softmax(sim / temperature) over it
 // and the argmax.  All reductions have a fixed order, so results are
 // bit-reproducible run to run.
+//
+// match_rep_kernel is the same step with rank-r_C representations in place of
+// mean keys (listing, Figure 2 and Figure 13): per unit it reads the query
+// representation Rq [d, r_C] and each anchor's Ra [d, r_C] into shared memory
+// and forms sim_a = |Rq^T Ra|_F^2 / (|Rq^T Rq|_F |Ra^T Ra|_F), the cosine of
+// the two rank-r_C key-Gram approximations, then the same top-k softmax.
 #include <cuda_bf16.h>
 
 #include "kvc_internal.h"
@@ -42,6 +48,31 @@ __device__ __forceinline__ void add_vec(float (&acc)[8], const uint4& v, float) 
   const float* p = reinterpret_cast<const float*>(&v);
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc[i] += p[i];
+}
+
+// Warp 0: weights = softmax(sim / temperature) over the top_k anchors
+// ordered by (-sim, index), 0 elsewhere; best = the lowest index of the max.
+__device__ void weights_from_sims(const float* sims, int A, int top_k, float inv_temperature,
+                                  float* weights, int32_t* best) {
+  const int lane = threadIdx.x & 31;
+  const bool valid = lane < A;
+  const float sim = valid ? sims[lane] : -INFINITY;
+  int rank = 0;
+  for (int b = 0; b < A; ++b) {
+    const float sb = sims[b];
+    rank += (sb > sim || (sb == sim && b < lane)) ? 1 : 0;
+  }
+  const bool kept = valid && rank < top_k;
+  // the maximum similarity sits at rank 0
+  const unsigned is_best = __ballot_sync(0xffffffffu, valid && rank == 0);
+  const int best_idx = __ffs(is_best) - 1;
+  const float top = sims[best_idx];
+  const float e = kept ? expf((sim - top) * inv_temperature) : 0.0f;
+  float den = e;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  if (valid) weights[lane] = kept ? e / den : 0.0f;
+  if (lane == 0) *best = best_idx;
 }
 
 template <typename T>
@@ -138,29 +169,109 @@ __global__ void __launch_bounds__(kMatchThreads)
     }
   }
   __syncthreads();
-  if (warp == 0) {
-    const bool valid = lane < a.A;
-    const float sim = valid ? sims[lane] : -INFINITY;
-    int rank = 0;
-    for (int b = 0; b < a.A; ++b) {
-      const float sb = sims[b];
-      rank += (sb > sim || (sb == sim && b < lane)) ? 1 : 0;
-    }
-    const bool kept = valid && rank < a.top_k;
-    // the maximum similarity sits at rank 0
-    const unsigned is_best = __ballot_sync(0xffffffffu, valid && rank == 0);
-    const int best_idx = __ffs(is_best) - 1;
-    const float top = sims[best_idx];
-    float e = kept ? expf((sim - top) * a.inv_temperature) : 0.0f;
-    float den = e;
+  if (warp == 0)
+    weights_from_sims(sims, a.A, a.top_k, a.inv_temperature, a.weights + uoff * a.A,
+                      a.best + uoff);
+}
+
+struct MatchRepArgs {
+  const float* query;             // [units, d, rc]
+  const float* anchors;           // [units, A, d, rc]
+  float* weights;                 // [units, A]
+  int32_t* best;                  // [units]
+  int32_t d, rc, A, top_k;
+  float inv_temperature;
+};
+
+// Block-wide fixed-order sum of one value per thread (result in every thread).
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    if (valid) a.weights[uoff * a.A + lane] = kept ? e / den : 0.0f;
-    if (lane == 0) a.best[uoff] = best_idx;
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.0f;
+  for (int w = 0; w < kMatchThreads / 32; ++w) t += red[w];
+  return t;
+}
+
+__global__ void __launch_bounds__(kMatchThreads) match_rep_kernel(const MatchRepArgs a) {
+  extern __shared__ float4 rsm4[];
+  float* Rq = reinterpret_cast<float*>(rsm4);      // [d][rc]
+  const int n = a.d * a.rc;
+  float* Ra = Rq + n;                              // [d][rc]
+  __shared__ float sims[32];
+  __shared__ float red[kMatchThreads / 32];
+  const int tid = threadIdx.x;
+  const int64_t unit = blockIdx.x;
+  const int rc = a.rc, d = a.d, ne = rc * rc;
+
+  const float4* q4 = reinterpret_cast<const float4*>(a.query + unit * n);
+  for (int i = tid; i < n / 4; i += kMatchThreads) rsm4[i] = __ldg(q4 + i);
+  __syncthreads();
+  // |Rq^T Rq|_F^2: thread handles Gram entries e = tid, tid + 256, ...
+  float v = 0.0f;
+  for (int e = tid; e < ne; e += kMatchThreads) {
+    const int i = e / rc, j = e - (e / rc) * rc;
+    float g = 0.0f;
+    for (int c = 0; c < d; ++c) g = fmaf(Rq[c * rc + i], Rq[c * rc + j], g);
+    v = fmaf(g, g, v);
   }
+  const float gqq = block_sum(v, red);
+  for (int an = 0; an < a.A; ++an) {
+    const float4* a4 = reinterpret_cast<const float4*>(a.anchors + (unit * a.A + an) * n);
+    float4* ra4 = reinterpret_cast<float4*>(Ra);
+    for (int i = tid; i < n / 4; i += kMatchThreads) ra4[i] = __ldg(a4 + i);
+    __syncthreads();
+    float vqa = 0.0f, vaa = 0.0f;
+    for (int e = tid; e < ne; e += kMatchThreads) {
+      const int i = e / rc, j = e - (e / rc) * rc;
+      float gqa = 0.0f, gaa = 0.0f;
+      for (int c = 0; c < d; ++c) {
+        const float raj = Ra[c * rc + j];
+        gqa = fmaf(Rq[c * rc + i], raj, gqa);
+        gaa = fmaf(Ra[c * rc + i], raj, gaa);
+      }
+      vqa = fmaf(gqa, gqa, vqa);
+      vaa = fmaf(gaa, gaa, vaa);
+    }
+    const float sqa = block_sum(vqa, red);
+    const float saa = block_sum(vaa, red);
+    if (tid == 0)
+      sims[an] = (gqq > 0.0f && saa > 0.0f) ? sqa / (sqrtf(gqq) * sqrtf(saa)) : 0.0f;
+    __syncthreads();   // Ra is overwritten by the next anchor
+  }
+  if ((tid >> 5) == 0)
+    weights_from_sims(sims, a.A, a.top_k, a.inv_temperature, a.weights + unit * a.A,
+                      a.best + unit);
 }
 
 }  // namespace
+
+cudaError_t launch_match_rep(const Dims& dm, const float* query_rep, const float* anchor_reps,
+                             int r_c, int top_k, float temperature, float* weights, int32_t* best,
+                             cudaStream_t stream) {
+  MatchRepArgs a{};
+  a.query = query_rep;
+  a.anchors = anchor_reps;
+  a.weights = weights;
+  a.best = best;
+  a.d = dm.d;
+  a.rc = r_c;
+  a.A = dm.A;
+  a.top_k = top_k;
+  a.inv_temperature = 1.0f / temperature;
+  const int64_t units = dm.units();
+  if (units <= 0) return cudaSuccess;
+  if (units > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>(2) * dm.d * r_c * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(match_rep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  match_rep_kernel<<<static_cast<unsigned>(units), kMatchThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_match(const Dims& dm, const SegTable& seg, kvc_dtype dtype, const View& refK,
                          const float* summaries, int top_k, float temperature, float* weights,

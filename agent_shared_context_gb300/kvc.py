@@ -44,7 +44,8 @@ KVC_F32 = 1
 EXPORTS = ("kvc_version", "kvc_status_string", "kvc_last_error",
            "kvc_build_states_workspace", "kvc_build_states", "kvc_match_anchors",
            "kvc_apply_correction", "kvc_chain_edge_workspace", "kvc_chain_edge",
-           "kvc_selftest_bounded_wait", "kvc_chain_edge_noalloc", "kvc_pool_insert")
+           "kvc_selftest_bounded_wait", "kvc_chain_edge_noalloc", "kvc_pool_insert",
+           "kvc_build_representation", "kvc_match_representation")
 
 KVC_NOALLOC_MAX_UNITS = 262144
 
@@ -77,7 +78,9 @@ class kvc_params(ctypes.Structure):
                 ("power_iters", ctypes.c_int32), ("n_anchors", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("energy_frac", ctypes.c_float),
                 ("temperature", ctypes.c_float), ("tau", ctypes.c_float),
-                ("select_mode", ctypes.c_int32), ("reuse_ratio", ctypes.c_float)]
+                ("select_mode", ctypes.c_int32), ("reuse_ratio", ctypes.c_float),
+                ("summary_mode", ctypes.c_int32), ("rank_c", ctypes.c_int32),
+                ("omega_c", ctypes.c_void_p)]
 
 
 _VIEW = kvc_cache_view
@@ -113,6 +116,10 @@ lib.kvc_chain_edge_noalloc.restype = _ST
 lib.kvc_chain_edge_noalloc.argtypes = [ctypes.c_int32, _SEG_P, _PRM_P, _VIEW, _VIEW, _VP, _VP, _VP,
                                        _VP, _VP, _VIEW, _VIEW, _VIEW, _VIEW, _VP, _VP, _VP, _VP,
                                        _VP, _VP]
+lib.kvc_build_representation.restype = _ST
+lib.kvc_build_representation.argtypes = [_SEG_P, _PRM_P, _VIEW, _VP, _VP, _VP, _VP, _VP]
+lib.kvc_match_representation.restype = _ST
+lib.kvc_match_representation.argtypes = [_SEG_P, _PRM_P, _VP, _VP, _VP, _VP, _VP, _VP]
 lib.kvc_selftest_bounded_wait.restype = _ST
 lib.kvc_selftest_bounded_wait.argtypes = [ctypes.c_int32, _VP, _VP]
 
@@ -187,17 +194,27 @@ class Segments:
 
 def params(rank: int = 32, oversample: int = 8, power_iters: int = 2, n_anchors: int = 8,
            top_k: int = 0, energy_frac: float = 0.9, temperature: float = 0.1,
-           tau: float = 0.32, reuse_ratio: Optional[float] = None) -> kvc_params:
-    """Method parameters; ``reuse_ratio`` switches to the reuse-ratio mode."""
+           tau: float = 0.32, reuse_ratio: Optional[float] = None,
+           rank_c: Optional[int] = None, omega_c: Ptr = None) -> kvc_params:
+    """Method parameters; ``reuse_ratio`` switches to the reuse-ratio mode,
+    ``rank_c`` (with the device test matrix ``omega_c`` [d, rank_c +
+    oversample]) to rank-r_C anchor representations.  The returned struct
+    holds omega_c's raw address: keep the tensor alive while it is used."""
     return kvc_params(rank, oversample, power_iters, n_anchors,
                       top_k if top_k > 0 else n_anchors, energy_frac, temperature, tau,
                       0 if reuse_ratio is None else 1,
-                      0.0 if reuse_ratio is None else float(reuse_ratio))
+                      0.0 if reuse_ratio is None else float(reuse_ratio),
+                      0 if rank_c is None else 1, 0 if rank_c is None else int(rank_c),
+                      _addr(omega_c))
 
 
-def params_from_workload(wl, **over) -> kvc_params:
+def params_from_workload(wl, omega_c: Ptr = None, **over) -> kvc_params:
+    """Parameters of a synthetic workload; rank-mode workloads need their
+    omega_c tensor (``WorkloadInputs.omega_c``)."""
     kw = dict(rank=wl.r, oversample=wl.oversample, power_iters=wl.power_iters, n_anchors=wl.A,
               top_k=wl.k_top, energy_frac=wl.energy_frac, temperature=wl.temperature, tau=wl.tau)
+    if getattr(wl, "summary_mode", "mean") == "rank":
+        kw.update(rank_c=wl.rank_c, omega_c=omega_c)
     kw.update(over)
     return params(**kw)
 
@@ -260,6 +277,24 @@ def kvc_match_anchors(seg: Segments, prm: kvc_params, ref_K, summaries: Ptr, wei
                                _addr(weights), _addr(best), _addr(query), _addr(dev_status),
                                _stream(stream))
     return _done(st, "kvc_match_anchors", check)
+
+
+def kvc_build_representation(seg: Segments, prm: kvc_params, cache_K, rep: Ptr,
+                             rep_sigma: Ptr = None, rep_eff_rank: Ptr = None,
+                             dev_status: Ptr = None, stream=None, check: bool = True) -> int:
+    st = lib.kvc_build_representation(seg.ref, ctypes.byref(prm), _v(cache_K), _addr(rep),
+                                      _addr(rep_sigma), _addr(rep_eff_rank), _addr(dev_status),
+                                      _stream(stream))
+    return _done(st, "kvc_build_representation", check)
+
+
+def kvc_match_representation(seg: Segments, prm: kvc_params, query_rep: Ptr, anchor_reps: Ptr,
+                             weights: Ptr, best: Ptr, dev_status: Ptr = None, stream=None,
+                             check: bool = True) -> int:
+    st = lib.kvc_match_representation(seg.ref, ctypes.byref(prm), _addr(query_rep),
+                                      _addr(anchor_reps), _addr(weights), _addr(best),
+                                      _addr(dev_status), _stream(stream))
+    return _done(st, "kvc_match_representation", check)
 
 
 def kvc_apply_correction(seg: Segments, prm: kvc_params, ref_K, ref_V, U_K: Ptr, W_K: Ptr,

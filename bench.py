@@ -179,8 +179,12 @@ def _oracle_sample(wl, seconds_hint: float = 20.0):
     if sub.build_slot >= 0:
         build = dict(slot=sub.build_slot, r=sub.r, omega=inp.omega.double().numpy(),
                      q=sub.power_iters, frac=sub.energy_frac)
+    rep = None
+    if sub.summary_mode == "rank":
+        summ = [e.reps.double().numpy() for e in inp.edges]
+        rep = dict(r_c=sub.rank_c, omega=inp.omega_c.double().numpy(), q=sub.power_iters)
     t0 = time.perf_counter()
-    O.chain(EK, EV, seg, states, summ, sub.k_top, sub.temperature, sub.tau, build=build)
+    O.chain(EK, EV, seg, states, summ, sub.k_top, sub.temperature, sub.tau, build=build, rep=rep)
     dt = time.perf_counter() - t0
     tokens = n * sub.edges * (n_units / units_total)
     desc = ("oracle chain over %d edges of one %d-token segment, %d of %d (layer, head) "
@@ -250,7 +254,7 @@ def run_kvc(args, wl):
     for _ in range(max(args.warmup, 3)):
         runner.run()
     torch.cuda.synchronize(dev)
-    launches_per_step = wl.edges * (4 + (1 if runner.build else 0))
+    launches_per_step = wl.edges * (4 + (1 if runner.build else 0) + (1 if runner.rank_mode else 0))
 
     barrier()
     torch.cuda.synchronize(dev)
@@ -331,6 +335,25 @@ def run_kvc(args, wl):
                    "tensor_path": ("M = delta^T delta on tcgen05 (split bf16)" if tc
                                    else "FP32 FMA")}
 
+    # ---- rank-r_C representations of the held keys (one launch per edge), timed alone
+    representation = None
+    if runner.rank_mode:
+        qrep = torch.empty((wl.S, wl.L, wl.H, wl.d, wl.rank_c), device=dev)
+        evr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(3)]
+        for i in range(4):
+            if i >= 1:
+                evr[i - 1][0].record(stream)
+            kvc.kvc_build_representation(seg, prm, inp.exact_K[0], qrep, None, None,
+                                         runner.dev_status)
+            if i >= 1:
+                evr[i - 1][1].record(stream)
+        torch.cuda.synchronize(dev)
+        r_ms = statistics.mean(a.elapsed_time(b) for a, b in evr)
+        representation = {"kernel": "build_tc_kernel (representation mode)", "launch_ms": r_ms,
+                          "units": wl.S * wl.L * wl.H, "rank_c": wl.rank_c,
+                          "key_bytes_per_launch": wl.ph_tokens * wl.L * wl.H * wl.d * ebytes}
+
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e and world == 1:
@@ -356,6 +379,9 @@ def run_kvc(args, wl):
         "builder": builder,
         "e2e": e2e,
     }
+    if representation is not None:
+        line["representation"] = representation
+        line["config"]["summary"] = "rank-%d representations" % wl.rank_c
     if rank == 0 and not args.no_cpu_baseline:
         v, dt, desc = _oracle_sample(wl)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": _blas_threads(),
@@ -383,7 +409,8 @@ def _e2e(args, wl, inp, runner, dev):
     pin(inp.exact_K[0])
     pin(inp.exact_V[0])
     for j, e in enumerate(inp.edges, start=1):
-        for t in (e.U_K, e.W_K, e.U_V, e.W_V, e.summaries, inp.exact_K[j], inp.exact_V[j]):
+        summaries = e.reps if runner.rank_mode else e.summaries
+        for t in (e.U_K, e.W_K, e.U_V, e.W_V, summaries, inp.exact_K[j], inp.exact_V[j]):
             pin(t)
     last = runner.edges[wl.edges]
     outs = [last.out_K, last.out_V] + [runner.edges[j].score for j in range(1, wl.edges + 1)] + \

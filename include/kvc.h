@@ -35,7 +35,17 @@
  *     score > tau; a zero reference scores 0 (zero C) or +inf;
  *   - effective rank of a state uses the l singular values of the sketch
  *     against |delta|_F^2 and is l + 1 when they retain less than the
- *     fraction.
+ *     fraction;
+ *   - rank-r_C representation of a segment's keys K [n, d] (listing, Figure 2:
+ *     the base cache's effective rank; Figure 13: (r_C, r_Delta) = (32, 32),
+ *     "Full" = uncompressed): Rep = W_C diag(sigma_C) [d, r_C], the r_C
+ *     leading right singular directions of K scaled by their singular values,
+ *     from the same randomized factorisation as the delta states with the
+ *     test matrix omega_c.  Rep Rep^T approximates the key Gram K^T K.  Two
+ *     representations are compared by the cosine of their Gram
+ *     approximations, |Rq^T Ra|_F^2 / (|Rq^T Rq|_F |Ra^T Ra|_F) (0 if either
+ *     is zero), which replaces the cosine of mean keys when
+ *     summary_mode == 1.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -73,6 +83,10 @@
  * omega                [d, l]           float32, l = rank + oversample
  * sigma                [S, L, H, 2, l]  float32 (K part then V part)
  * eff_rank             [S, L, H, 2]     int32
+ * rep (query)          [S, L, H, d, r_C]     float32
+ * anchor reps          [S, L, H, A, d, r_C]  float32 (summaries, mode 1)
+ * rep_sigma            [S, L, H, l_C]   float32
+ * rep_eff_rank         [S, L, H]        int32
  * U, W, caches share the dtype of the segment descriptor (bf16 or f32).
  */
 #ifndef KVC_H_
@@ -87,7 +101,7 @@ extern "C" {
 #endif
 
 #define KVC_VERSION_MAJOR 0
-#define KVC_VERSION_MINOR 1
+#define KVC_VERSION_MINOR 2
 
 typedef enum kvc_status {
   KVC_OK = 0,
@@ -147,6 +161,13 @@ typedef struct kvc_params {
                         /*    are reused, the rest -- largest scores, ties to   */
                         /*    the lower index -- fall back (listing, Figure 5)  */
   float reuse_ratio;    /* rho in [0, 1], read when select_mode == 1          */
+  int32_t summary_mode; /* 0: anchors carry mean keys [S, L, H, A, d];        */
+                        /* 1: anchors carry rank-r_C representations          */
+                        /*    [S, L, H, A, d, rank_c] (listing, Figures 2, 13) */
+  int32_t rank_c;       /* r_C, 1..64, read when summary_mode == 1; l_C =      */
+                        /* rank_c + oversample <= min(d, 64); needs d <= 128   */
+  const float* omega_c; /* DEVICE test matrix [d, l_C] of the representations, */
+                        /* read when summary_mode == 1                        */
 } kvc_params;
 
 /* Library version string, e.g. "0.1.0 sm_103a". */
@@ -210,12 +231,44 @@ kvc_status kvc_pool_insert(const kvc_segments* seg, const kvc_params* prm,
  *
  * query = mean of ref_K over the segment's tokens; sim_a = cos(query,
  * summaries[a]); weights = softmax(sim / temperature) over the top_k
- * anchors; best = argmax sim.  `query` may be NULL.
+ * anchors; best = argmax sim.  `query` may be NULL.  This is the
+ * summary_mode 0 match; summary_mode 1 is rejected (KVC_ERR_INVALID_ARGUMENT).
  * ------------------------------------------------------------------------- */
 kvc_status kvc_match_anchors(const kvc_segments* seg, const kvc_params* prm,
                              kvc_cache_view ref_K, const float* summaries,
                              float* weights, int32_t* best, float* query,
                              int32_t* dev_status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * kvc_build_representation -- rank-r_C representation of every PH segment's
+ * keys (listing, Figure 2 and Figure 13; reading above).
+ *
+ * For each (segment, layer, head): the keys of cache_K over the segment's
+ * rows are factored by the randomized subspace iteration of
+ * kvc_build_states (test matrix prm->omega_c [d, l_C], q = power_iters),
+ * and rep[s, l, h] = W_C diag(sigma_C) [d, r_C] is written.  rep_sigma
+ * (the l_C sketch singular values) and rep_eff_rank (effective rank of the
+ * keys, fraction energy_frac of |K|_F^2, l_C + 1 when the sketch retains
+ * less) may be NULL.  Needs summary_mode == 1 parameters (rank_c, omega_c),
+ * d <= 128 and every segment len >= l_C.  Uses no workspace.
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_build_representation(const kvc_segments* seg, const kvc_params* prm,
+                                    kvc_cache_view cache_K, float* rep, float* rep_sigma,
+                                    int32_t* rep_eff_rank, int32_t* dev_status,
+                                    cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * kvc_match_representation -- match query representations to the anchors'
+ * representations (listing, Figure 1(b) with rank-r_C summaries).
+ *
+ * sim_a = |Rq^T Ra|_F^2 / (|Rq^T Rq|_F |Ra^T Ra|_F) per (segment, layer,
+ * head) from query_rep [S, L, H, d, r_C] and anchor_reps [S, L, H, A, d,
+ * r_C]; weights and best as kvc_match_anchors.  Needs summary_mode == 1.
+ * ------------------------------------------------------------------------- */
+kvc_status kvc_match_representation(const kvc_segments* seg, const kvc_params* prm,
+                                    const float* query_rep, const float* anchor_reps,
+                                    float* weights, int32_t* best, int32_t* dev_status,
+                                    cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * kvc_apply_correction -- fused correction and reliability check (listing,
@@ -244,14 +297,18 @@ kvc_status kvc_apply_correction(const kvc_segments* seg, const kvc_params* prm,
  *
  * edge == 0: agent A0's cache is exact; arguments are validated and nothing
  *   is launched or written.
- * edge >= 1: match (kvc_match_anchors), apply + score (kvc_apply_correction)
- *   with ref = the held cache of the previous agent, then every flagged
+ * edge >= 1: match (kvc_match_anchors; with summary_mode == 1
+ *   kvc_build_representation of ref_K then kvc_match_representation, and
+ *   `summaries` holds the anchors' representations), apply + score
+ *   (kvc_apply_correction) with ref = the held cache of the previous agent,
+ *   then every flagged
  *   segment's rows are copied bit-exactly from dense_K/dense_V when their base
  *   is non-NULL (the dense-prefill result); otherwise the corrected rows stay
  *   and the caller reads `fallback` to prefill those segments itself.  out
  *   becomes the held cache (the reference of the next edge); rows outside the
  *   PH segments are not touched.  `workspace` must hold
- *   kvc_chain_edge_workspace() bytes (per-unit norms), 256-byte aligned.
+ *   kvc_chain_edge_workspace() bytes (per-unit norms, and the query
+ *   representations in summary_mode 1), 256-byte aligned.
  * ------------------------------------------------------------------------- */
 size_t kvc_chain_edge_workspace(const kvc_segments* seg, const kvc_params* prm);
 kvc_status kvc_chain_edge(int32_t edge, const kvc_segments* seg, const kvc_params* prm,

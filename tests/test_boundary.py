@@ -244,3 +244,64 @@ def test_reuse_ratio_mode_validation():
     p.select_mode = 2
     assert a.apply(prm=p) == kvc.KVC_ERR_INVALID_ARGUMENT
     assert "select_mode" in kvc.lib.kvc_last_error().decode()
+
+
+def _rep_prm(rank_c=32, omega_c=FAKE, **kw):
+    base = dict(rank=32, oversample=8, power_iters=2, n_anchors=8, top_k=8)
+    base.update(kw)
+    return kvc.params(rank_c=rank_c, omega_c=omega_c, **base)
+
+
+def test_representation_mode_validation():
+    """Rank-r_C representations (summary_mode 1): every call below carries
+    one argument the host layer rejects."""
+    a = Args()
+    seg = a.seg
+
+    def build(**kw):
+        args = dict(seg=seg, prm=_rep_prm(), cache_K=a.ref_K, rep=FAKE, rep_sigma=None,
+                    rep_eff_rank=None, dev_status=FAKE)
+        args.update(kw)
+        return kvc.kvc_build_representation(stream=0, check=False, **args)
+
+    assert build(prm=a.prm) == kvc.KVC_ERR_INVALID_ARGUMENT              # summary_mode 0
+    assert build(prm=_rep_prm(rank_c=0)) == kvc.KVC_ERR_INVALID_ARGUMENT
+    assert build(prm=_rep_prm(rank_c=60)) == kvc.KVC_ERR_UNSUPPORTED      # 60 + 8 > 64
+    assert build(prm=_rep_prm(omega_c=None)) == kvc.KVC_ERR_INVALID_ARGUMENT
+    assert build(prm=_rep_prm(power_iters=9)) == kvc.KVC_ERR_INVALID_ARGUMENT
+    assert build(seg=_seg(lens=(300, 30))) == kvc.KVC_ERR_SHAPE          # 30 < l_C = 40
+    assert build(rep=None) == kvc.KVC_ERR_INVALID_ARGUMENT
+    assert build(rep=FAKE + 4) == kvc.KVC_ERR_ALIGNMENT
+    assert build(cache_K=_view(FAKE + 2)) == kvc.KVC_ERR_ALIGNMENT
+    wide = _seg(dtype="f32", d=256)
+    assert build(seg=wide, cache_K=_view(FAKE, d=256)) == kvc.KVC_ERR_UNSUPPORTED
+    assert "d <= 128" in kvc.lib.kvc_last_error().decode()
+
+    def match(**kw):
+        args = dict(seg=seg, prm=_rep_prm(), query_rep=FAKE, anchor_reps=FAKE, weights=FAKE,
+                    best=FAKE, dev_status=FAKE)
+        args.update(kw)
+        return kvc.kvc_match_representation(stream=0, check=False, **args)
+
+    assert match(prm=a.prm) == kvc.KVC_ERR_INVALID_ARGUMENT
+    assert match(query_rep=None) == kvc.KVC_ERR_INVALID_ARGUMENT
+    assert match(anchor_reps=FAKE + 8) == kvc.KVC_ERR_ALIGNMENT
+    assert match(prm=_rep_prm(top_k=9)) == kvc.KVC_ERR_INVALID_ARGUMENT
+    p = _rep_prm()
+    p.summary_mode = 2
+    assert match(prm=p) == kvc.KVC_ERR_INVALID_ARGUMENT
+    # the mean-key match refuses representation parameters
+    assert kvc.kvc_match_anchors(seg, _rep_prm(), a.ref_K, FAKE, FAKE, FAKE, None, FAKE, stream=0,
+                                 check=False) == kvc.KVC_ERR_INVALID_ARGUMENT
+
+
+def test_chain_edge_workspace_in_representation_mode():
+    a = Args()
+    prm = _rep_prm()
+    units = 2 * 2 * 2
+    need = kvc.kvc_chain_edge_workspace(a.seg, prm)
+    r256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    assert need == r256(units * 4 * 4) + r256(units * 128 * 32 * 4)
+    assert _chain(a, 1, need - 1, prm=prm) == kvc.KVC_ERR_WORKSPACE
+    assert _chain(a, 1, need, prm=_rep_prm(omega_c=None)) == kvc.KVC_ERR_INVALID_ARGUMENT
+    assert _chain(a, 1, need, prm=prm, summaries=FAKE + 4) == kvc.KVC_ERR_ALIGNMENT
