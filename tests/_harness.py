@@ -23,7 +23,9 @@ def oracle_inputs(wl: synth.Workload, inp: synth.WorkloadInputs):
     EV = [np64(t) for t in inp.exact_V]
     states = [None if e is None else O.States(np64(e.U_K), np64(e.W_K), np64(e.U_V), np64(e.W_V))
               for e in inp.edges]
-    summ = [None if e is None else np64(e.summaries) for e in inp.edges]
+    # rank-r_C workloads match against the anchors' representations
+    rank = wl.summary_mode == "rank"
+    summ = [None if e is None else np64(e.reps if rank else e.summaries) for e in inp.edges]
     return seg, EK, EV, states, summ
 
 
@@ -34,19 +36,25 @@ def oracle_chain(wl: synth.Workload, inp: synth.WorkloadInputs, use_dense: bool 
     if build:
         b = dict(slot=wl.build_slot, r=wl.r, omega=np64(inp.omega), q=wl.power_iters,
                  frac=wl.energy_frac)
+    rep = None
+    if wl.summary_mode == "rank":
+        rep = dict(r_c=wl.rank_c, omega=np64(inp.omega_c), q=wl.power_iters)
     res = O.chain(EK, EV, seg, states, summ, wl.k_top, wl.temperature, wl.tau,
-                  use_dense=use_dense, build=b)
+                  use_dense=use_dense, build=b, rep=rep)
     return res, (seg, EK, EV, states, summ)
 
 
 def sim_gaps(query: np.ndarray, summaries: np.ndarray) -> np.ndarray:
-    """Gap between the two largest cosine similarities per unit (oracle)."""
-    S, L, H, A, d = summaries.shape
+    """Gap between the two largest similarities per unit (oracle): cosine of
+    mean keys, or the Gram cosine of representations when ``summaries`` is
+    [S, L, H, A, d, r_C]."""
+    S, L, H, A = summaries.shape[:4]
+    sim = O.rep_similarity if summaries.ndim == 6 else O.cosine
     gaps = np.full((S, L, H), np.inf)
     for s in range(S):
         for l in range(L):
             for h in range(H):
-                sims = sorted((O.cosine(query[s, l, h], summaries[s, l, h, a]) for a in range(A)),
+                sims = sorted((sim(query[s, l, h], summaries[s, l, h, a]) for a in range(A)),
                               reverse=True)
                 if A > 1:
                     gaps[s, l, h] = sims[0] - sims[1]

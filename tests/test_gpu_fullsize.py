@@ -41,10 +41,12 @@ def restrict(wl, inp, q, segs):
             U_V=e.U_V.index_select(0, idx)[:, :, :, :Tm].contiguous(),
             W_V=e.W_V.index_select(0, idx),
             summaries=e.summaries.index_select(0, idx),
-            planted=e.planted[segs]))
+            planted=e.planted[segs],
+            reps=None if e.reps is None else e.reps.index_select(0, idx)))
     return sub, WorkloadInputs(wl=sub, exact_K=[E[q:q + 1] for E in inp.exact_K],
                                exact_V=[E[q:q + 1] for E in inp.exact_V], edges=edges,
-                               omega=inp.omega, planted_ratio=inp.planted_ratio)
+                               omega=inp.omega, planted_ratio=inp.planted_ratio,
+                               omega_c=inp.omega_c)
 
 
 def _compare(wl, runner, sub, sub_inp, q, segs, build):
@@ -134,6 +136,19 @@ def test_vl_full_size_sampled_segments_with_tail():
     segs = [2, 5, 17]                   # visual-block segments and the 296-token tail
     sub, sub_inp = restrict(wl, inp, 0, segs)
     _compare(wl, runner, sub, sub_inp, 0, segs, build=False)
+
+
+def test_llama2k_rank_representations_full_size_sampled_request():
+    """llama2k with rank-32 anchor representations: the whole batch on the
+    GPU (representations of 2,560 units of 2,048 held keys per edge), one
+    request recomputed by the oracle."""
+    wl = synth.workload("llama2k-rc32")
+    inp, runner = _run(wl)
+    planted = inp.edges[0].planted
+    q = int(torch.nonzero(planted)[0]) if bool(planted.any()) else 0
+    segs = [s for s in range(wl.S) if wl.seg_request[s] == q]
+    sub, sub_inp = restrict(wl, inp, q, segs)
+    _compare(wl, runner, sub, sub_inp, q, segs, build=False)
 
 
 def test_longctx_full_size_with_builder_sampled_segments():
