@@ -36,6 +36,7 @@ class EdgeOutputs:
     fallback: torch.Tensor
     sigma: Optional[torch.Tensor] = None
     eff_rank: Optional[torch.Tensor] = None
+    ksum: Optional[torch.Tensor] = None       # held-key column sums for the next edge
 
 
 def ph_row_mask(wl: Workload, device) -> torch.Tensor:
@@ -49,7 +50,7 @@ def ph_row_mask(wl: Workload, device) -> torch.Tensor:
 class ChainRunner:
     def __init__(self, wl: Workload, inp: WorkloadInputs, device="cuda", use_dense: bool = True,
                  poison_ph: bool = False, stream: Optional[torch.cuda.Stream] = None,
-                 build: Optional[bool] = None, fixed_ref=None):
+                 build: Optional[bool] = None, fixed_ref=None, carry_ksum: bool = True):
         self.wl = wl
         self.inp = inp
         self.device = torch.device(device)
@@ -63,6 +64,9 @@ class ChainRunner:
         # omega_c's address (inp keeps the tensor alive)
         self.rank_mode = wl.summary_mode == "rank"
         self.prm = kvc.params_from_workload(wl, omega_c=inp.omega_c if self.rank_mode else None)
+        # edge j hands the column sums of the keys it leaves to edge j + 1, whose
+        # match then reads no key rows (mean-key mode, chained references only)
+        self.carry_ksum = carry_ksum and not self.rank_mode and fixed_ref is None
         S, L, H, A = wl.S, wl.L, wl.H, wl.A
         dev = self.device
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -91,6 +95,8 @@ class ChainRunner:
             if self.build:
                 eo.sigma = torch.empty((S, L, H, 2, wl.l), dtype=torch.float32, device=dev)
                 eo.eff_rank = torch.empty((S, L, H, 2), dtype=torch.int32, device=dev)
+            if self.carry_ksum and j < wl.edges:
+                eo.ksum = torch.empty((S, L, H, 4, wl.d), dtype=torch.float32, device=dev)
             self.edges.append(eo)
 
     def held(self, j: int):
@@ -116,9 +122,11 @@ class ChainRunner:
         dK = inp.exact_K[j] if self.use_dense else None
         dV = inp.exact_V[j] if self.use_dense else None
         summaries = e.reps if self.rank_mode else e.summaries
+        ksum_in = self.edges[j - 1].ksum if (self.carry_ksum and j > 1) else None
         kvc.kvc_chain_edge(j, self.seg, self.prm, refK, refV, summaries, e.U_K, e.W_K, e.U_V,
                            e.W_V, dK, dV, eo.out_K, eo.out_V, eo.weights, eo.best, eo.score,
-                           eo.fallback, self.workspace, self.dev_status, stream=self.stream)
+                           eo.fallback, self.workspace, self.dev_status, stream=self.stream,
+                           ksum_in=ksum_in, ksum_out=eo.ksum)
 
     def run(self) -> None:
         for j in range(1, self.wl.edges + 1):

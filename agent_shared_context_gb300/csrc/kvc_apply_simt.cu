@@ -186,11 +186,25 @@ struct CopyArgs {
   char* dst[2];
   int64_t ss[2][4];
   int64_t ds[2][4];
+  float* ksum;          // bf16 only: [units, 4, d] column sums of the copied K rows, or nullptr
   int32_t L, H, row_bytes, elem;
 };
 
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& v) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(p[i]);
+    acc[2 * i] += f.x;
+    acc[2 * i + 1] += f.y;
+  }
+}
+
 // grid = (L*H*2, S): one CTA copies the rows of one (segment, layer, head,
-// K|V) when the segment is flagged; 16-byte vector copies.
+// K|V) when the segment is flagged; 16-byte vector copies.  With ksum (bf16,
+// 256 threads a multiple of the 16-byte chunks per row, so every thread stays
+// on one chunk of 8 columns) the K copies also sum their columns: per-thread
+// sums in row order, then a fixed-order sum over the row groups.
 __global__ void __launch_bounds__(256)
     fallback_copy_kernel(const CopyArgs a, const __grid_constant__ SegTable seg,
                          const uint8_t* __restrict__ fallback) {
@@ -208,6 +222,8 @@ __global__ void __launch_bounds__(256)
   const int vec_per_row = a.row_bytes / 16;
   const int total = seg.len[s] * vec_per_row;
   const int step = blockDim.x;
+  const bool sums = a.ksum != nullptr && kv == 0 && e == 2;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   // four independent 16-byte loads in flight per thread
   int i = threadIdx.x;
   for (; i + 3 * step < total; i += 4 * step) {
@@ -223,12 +239,34 @@ __global__ void __launch_bounds__(256)
       const int k = i + u * step;
       const int t = k / vec_per_row, c = k % vec_per_row;
       reinterpret_cast<uint4*>(dst + t * a.ds[kv][3] * e)[c] = v[u];
+      if (sums) add_bf16x8(acc, v[u]);
     }
   }
   for (; i < total; i += step) {
     const int t = i / vec_per_row, c = i % vec_per_row;
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + t * a.ss[kv][3] * e) + c);
     reinterpret_cast<uint4*>(dst + t * a.ds[kv][3] * e)[c] = v;
+    if (sums) add_bf16x8(acc, v);
+  }
+  if (sums) {
+    // thread tid holds columns 8 * (tid % vec_per_row) .. + 7 of row group tid / vec_per_row
+    __shared__ float red[256 * 8];
+    const int d = vec_per_row * 8;
+    const int groups = step / vec_per_row;
+    const int g = threadIdx.x / vec_per_row, c8 = (threadIdx.x % vec_per_row) * 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) red[g * d + c8 + j] = acc[j];
+    __syncthreads();
+    const int64_t unit = (static_cast<int64_t>(s) * a.L + l) * a.H + h;
+    float* out = a.ksum + unit * 4 * d;
+    for (int c = threadIdx.x; c < d; c += step) {
+      float t = 0.0f;
+      for (int gg = 0; gg < groups; ++gg) t += red[gg * d + c];
+      out[c] = t;
+      out[d + c] = 0.0f;
+      out[2 * d + c] = 0.0f;
+      out[3 * d + c] = 0.0f;
+    }
   }
 }
 
@@ -299,7 +337,7 @@ cudaError_t launch_select_ratio(const Dims& dm, const float* score, int n_reuse,
 
 cudaError_t launch_fallback_copy(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
                                  const View densev[2], const View outv[2],
-                                 const uint8_t* fallback, cudaStream_t stream) {
+                                 const uint8_t* fallback, cudaStream_t stream, float* ksum) {
   CopyArgs a{};
   for (int kv = 0; kv < 2; ++kv) {
     a.src[kv] = static_cast<const char*>(densev[kv].base);
@@ -317,6 +355,8 @@ cudaError_t launch_fallback_copy(const Dims& dm, const SegTable& seg, kvc_dtype 
   a.H = dm.H;
   a.elem = dtype == KVC_BF16 ? 2 : 4;
   a.row_bytes = dm.d * a.elem;
+  // the column sums need every thread on a fixed 16-byte chunk of a row
+  a.ksum = (dtype == KVC_BF16 && 256 % (a.row_bytes / 16) == 0) ? ksum : nullptr;
   if (dm.S <= 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>(dm.L * dm.H * 2), static_cast<unsigned>(dm.S));
   fallback_copy_kernel<<<grid, 256, 0, stream>>>(a, seg, fallback);

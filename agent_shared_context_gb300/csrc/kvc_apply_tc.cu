@@ -15,6 +15,7 @@
 //                      K = A*r in steps of 16, accumulating in TMEM (two
 //                      accumulator buffers so tile t+1's MMAs overlap tile
 //                      t's epilogue);
+//   warp 7             the K output tiles' column sums (below);
 //   warps 2-5          fold the weights into W in place (bf16, RNE) once per
 //                      item; per tile read the fp32 accumulator rows from
 //                      TMEM (thread = token row), add the ref row from shared
@@ -25,6 +26,15 @@
 //
 // Per-item norms are reduced in a fixed order and written to partial[unit,
 // kv] / partial[unit, 2 + kv]; K4 turns them into the segment score.
+//
+// Warp 7 sums the columns of every finished K output tile (ksum != nullptr):
+// the held keys the next workflow edge mean-pools into its query (listing,
+// Figure 1(b)-(c)), so that edge reads no key rows to match.  It waits for the
+// epilogue to have written a tile in place, reads its rows from shared memory
+// (lane = D/32 adjacent columns, rows in order, rows past the segment
+// skipped), and is the second arrival that frees the ref buffer; the item's
+// totals go to ksum[unit, 0, :] (quadrants 1-3 zero).  Off the epilogue's
+// path, it costs the HBM-bound pipeline nothing but a later buffer release.
 //
 // Every wait is bounded (kWaitLimitNs); a wait that expires stores
 // KVC_ERR_DEVICE_TIMEOUT into *dev_status, raises a CTA-wide abort flag so
@@ -45,7 +55,7 @@ using namespace ptx;
 constexpr int kBM = 128;                   // tokens per tile (MMA M)
 constexpr int kChunk = 64;                 // bf16 per 128-byte swizzled row
 constexpr int kUStageBytes = kBM * 128;    // one U chunk: 128 rows x 128 B
-constexpr int kThreads = 224;
+constexpr int kThreads = 256;
 constexpr int kMaxUStages = 8;
 constexpr int kMaxRefBufs = 3;
 constexpr int kEpiThreads = 128;
@@ -62,6 +72,7 @@ struct TcArgs {
   int64_t os[2][4];          // out element strides (req, layer, head, tok)
   const float* weights;      // [units, A]
   float* partial;            // [units, 4]
+  float* ksum;               // [units, 4, D] column sums of the K output rows, or nullptr
   int32_t* dev_status;
   int32_t L, H, A, r, K, KC, n_items, n_ustages, n_refbufs;
 };
@@ -71,6 +82,7 @@ struct Bars {
   uint64_t acc_full[2], acc_empty[2];
   uint64_t u_full[kMaxUStages], u_empty[kMaxUStages];
   uint64_t ref_full[kMaxRefBufs], ref_empty[kMaxRefBufs];
+  uint64_t tile_done[kMaxRefBufs];   // the epilogue has written the output tile in place
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t epi_ok[2];
@@ -81,10 +93,13 @@ struct Item {
   int unit, kv, s, l, h, req, start, len, ntiles;
 };
 
+// Items run all K halves first, then all V halves: with a persistent grid
+// every CTA gets about as many K items (which carry the key sums) as V items.
 __device__ __forceinline__ Item decode_item(int it, const TcArgs& a, const SegTable& seg) {
   Item x;
-  x.kv = it & 1;
-  x.unit = it >> 1;
+  const int units = a.n_items >> 1;
+  x.kv = it >= units ? 1 : 0;
+  x.unit = it - x.kv * units;
   x.h = x.unit % a.H;
   x.l = (x.unit / a.H) % a.L;
   x.s = x.unit / (a.H * a.L);
@@ -161,7 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < NRB; ++i) {
       mbar_init(&bars->ref_full[i], 1);
-      mbar_init(&bars->ref_empty[i], 1);
+      mbar_init(&bars->ref_empty[i], 2);     // the store's release + the key-sum warp
+      mbar_init(&bars->tile_done[i], 1);
     }
     bars->abort_flag = 0;
     bars->epi_ok[0] = 1;
@@ -334,6 +350,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)mbar_wait_bounded(&bars->mma_drain, 0, kWaitLimitNs);
       }
     }
+  } else if (warp == 7) {
+    // ------------------------------------------------------ key column sums
+    constexpr int CPL = D / 32;               // adjacent columns per lane
+    const int c0 = lane * CPL;
+    const int sb = c0 / kChunk;               // 64-column sub-box of the tile
+    const int j16 = (c0 % kChunk) / 8;        // 16-byte unit within the 128-byte row
+    const int boff = (c0 % 8) * 2;            // byte offset within that unit
+    uint32_t rb = 0, rph = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x) {
+      const Item x = decode_item(it, a, seg);
+      const bool want = a.ksum != nullptr && x.kv == 0;
+      float cs[CPL];
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) cs[i] = 0.0f;
+      for (int t = 0; t < x.ntiles; ++t) {
+        const bool got = wait_or_abort(&bars->tile_done[rb], rph, bars, a.dev_status);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        if (want) {
+          const int rows_valid = min(kBM, x.len - t * kBM);
+          const uint8_t* rt = r_smem + rb * REFB + sb * (kBM * 128) + boff;
+#pragma unroll 4
+          for (int m = 0; m < rows_valid; ++m) {
+            const uint8_t* p = rt + m * 128 + ((j16 ^ (m & 7)) << 4);
+            if constexpr (CPL == 4) {
+              const uint2 w2 = *reinterpret_cast<const uint2*>(p);
+              const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2.x));
+              const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w2.y));
+              cs[0] += f0.x;
+              cs[1] += f0.y;
+              cs[2] += f1.x;
+              cs[3] += f1.y;
+            } else {
+              const uint32_t w1 = *reinterpret_cast<const uint32_t*>(p);
+              const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w1));
+              cs[0] += f0.x;
+              cs[1] += f0.y;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->ref_empty[rb]);
+        if (++rb == static_cast<uint32_t>(NRB)) {
+          rb = 0;
+          rph ^= 1u;
+        }
+      }
+      if (ok && want) {
+        float* dst = a.ksum + static_cast<int64_t>(x.unit) * 4 * D;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          dst[c0 + i] = cs[i];
+          dst[D + c0 + i] = 0.0f;
+          dst[2 * D + c0 + i] = 0.0f;
+          dst[3 * D + c0 + i] = 0.0f;
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int et = threadIdx.x - 64;          // 0..127
@@ -441,7 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         fence_proxy_async_smem();
         named_sync(1, kEpiThreads);
-        if (et == 0) mbar_arrive(&bars->acc_empty[b]);
+        if (et == 0) {
+          mbar_arrive(&bars->acc_empty[b]);
+          mbar_arrive(&bars->tile_done[rb]);
+        }
         if (rows_valid == kBM) {
           if (et == 0) {
 #pragma unroll
@@ -528,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 cudaError_t launch_d(const Dims& dm, const SegTable& seg, const View refv[2], const View outv[2],
                      const void* U[2], const void* W[2], const float* weights, float* partial,
-                     int32_t* dev_status, cudaStream_t stream) {
+                     float* ksum, int32_t* dev_status, cudaStream_t stream) {
   DeviceInfo di{};
   cudaError_t e = device_info(&di);
   if (e != cudaSuccess) return e;
@@ -611,6 +691,7 @@ cudaError_t launch_d(const Dims& dm, const SegTable& seg, const View refv[2], co
   }
   a.weights = weights;
   a.partial = partial;
+  a.ksum = ksum;
   a.dev_status = dev_status;
   a.L = dm.L;
   a.H = dm.H;
@@ -637,12 +718,12 @@ cudaError_t launch_d(const Dims& dm, const SegTable& seg, const View refv[2], co
 
 cudaError_t launch_apply_tc(const Dims& dm, const SegTable& seg, const View refv[2],
                             const View outv[2], const void* U[2], const void* W[2],
-                            const float* weights, float* partial, int32_t* dev_status,
-                            cudaStream_t stream) {
+                            const float* weights, float* partial, float* ksum,
+                            int32_t* dev_status, cudaStream_t stream) {
   if (dm.d == 128)
-    return launch_d<128>(dm, seg, refv, outv, U, W, weights, partial, dev_status, stream);
+    return launch_d<128>(dm, seg, refv, outv, U, W, weights, partial, ksum, dev_status, stream);
   if (dm.d == 64)
-    return launch_d<64>(dm, seg, refv, outv, U, W, weights, partial, dev_status, stream);
+    return launch_d<64>(dm, seg, refv, outv, U, W, weights, partial, ksum, dev_status, stream);
   return cudaErrorInvalidValue;
 }
 

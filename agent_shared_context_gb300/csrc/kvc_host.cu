@@ -494,7 +494,7 @@ static kvc_status apply_impl(const kvc_segments* seg, const kvc_params* prm, con
                              const void* W_K, const void* U_V, const void* W_V,
                              const float* weights, kvc_cache_view out_K, kvc_cache_view out_V,
                              float* partial, float* score, uint8_t* fallback,
-                             int32_t* dev_status, cudaStream_t stream) {
+                             int32_t* dev_status, cudaStream_t stream, float* ksum = nullptr) {
   const Dims dm = make_dims(seg, prm);
   const View rf[2] = {to_view(ref_K), to_view(ref_V)};
   const View ov[2] = {to_view(out_K), to_view(out_V)};
@@ -502,7 +502,7 @@ static kvc_status apply_impl(const kvc_segments* seg, const kvc_params* prm, con
   const void* Ws[2] = {W_K, W_V};
   cudaError_t e;
   if (seg->dtype == KVC_BF16)
-    e = launch_apply_tc(dm, tab, rf, ov, Us, Ws, weights, partial, dev_status, stream);
+    e = launch_apply_tc(dm, tab, rf, ov, Us, Ws, weights, partial, ksum, dev_status, stream);
   else
     e = launch_apply_simt(dm, tab, rf, ov, Us, Ws, weights, partial, stream);
   if (e != cudaSuccess) return cuda_fail(e, "correction apply launch");
@@ -522,7 +522,8 @@ kvc_status kvc_apply_correction(const kvc_segments* seg, const kvc_params* prm,
                                 const void* W_K, const void* U_V, const void* W_V,
                                 const float* weights, kvc_cache_view out_K,
                                 kvc_cache_view out_V, float* partial, float* score,
-                                uint8_t* fallback, int32_t* dev_status, cudaStream_t stream) {
+                                uint8_t* fallback, float* ksum_out, int32_t* dev_status,
+                                cudaStream_t stream) {
   static thread_local SegTable tab;
   KVC_TRY(check_segments(seg, &tab));
   KVC_TRY(check_params(seg, prm, true, false, false));
@@ -532,9 +533,19 @@ kvc_status kvc_apply_correction(const kvc_segments* seg, const kvc_params* prm,
   KVC_TRY(check_dev_ptr(score, "score"));
   KVC_TRY(check_dev_ptr(fallback, "fallback"));
   KVC_TRY(check_dev_ptr(dev_status, "dev_status"));
+  if (ksum_out != nullptr && (reinterpret_cast<uintptr_t>(ksum_out) & 3u))
+    return fail(KVC_ERR_ALIGNMENT, "ksum_out must be 4-byte aligned");
   if (seg->S == 0) return KVC_OK;
-  return apply_impl(seg, prm, tab, ref_K, ref_V, U_K, W_K, U_V, W_V, weights, out_K, out_V,
-                    partial, score, fallback, dev_status, stream);
+  const bool fused = ksum_out != nullptr && seg->dtype == KVC_BF16;
+  KVC_TRY(apply_impl(seg, prm, tab, ref_K, ref_V, U_K, W_K, U_V, W_V, weights, out_K, out_V,
+                     partial, score, fallback, dev_status, stream, fused ? ksum_out : nullptr));
+  if (ksum_out != nullptr && !fused) {
+    const cudaError_t e = launch_match(make_dims(seg, prm), tab, seg->dtype, to_view(out_K),
+                                       nullptr, 1, 1.0f, nullptr, nullptr, nullptr, dev_status,
+                                       stream, nullptr, ksum_out);
+    if (e != cudaSuccess) return cuda_fail(e, "key-sum launch");
+  }
+  return KVC_OK;
 }
 
 // --------------------------------------------------------------- chain
@@ -552,8 +563,9 @@ kvc_status kvc_chain_edge(int32_t edge, const kvc_segments* seg, const kvc_param
                           const void* U_K, const void* W_K, const void* U_V, const void* W_V,
                           kvc_cache_view dense_K, kvc_cache_view dense_V, kvc_cache_view out_K,
                           kvc_cache_view out_V, float* weights, int32_t* best, float* score,
-                          uint8_t* fallback, void* workspace, size_t workspace_bytes,
-                          int32_t* dev_status, cudaStream_t stream) {
+                          uint8_t* fallback, const float* ksum_in, float* ksum_out,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                          cudaStream_t stream) {
   static thread_local SegTable tab;
   if (edge < 0) return fail(KVC_ERR_INVALID_ARGUMENT, "edge = %d < 0", edge);
   KVC_TRY(check_segments(seg, &tab));
@@ -580,6 +592,19 @@ kvc_status kvc_chain_edge(int32_t edge, const kvc_segments* seg, const kvc_param
     if (overlap(ok, dk) || overlap(ok, dv) || overlap(ov, dk) || overlap(ov, dv))
       return fail(KVC_ERR_ALIAS, "out_K/out_V may not overlap dense_K/dense_V");
   }
+  if (ksum_in != nullptr || ksum_out != nullptr) {
+    if (prm->summary_mode != 0)
+      return fail(KVC_ERR_INVALID_ARGUMENT, "ksum_in / ksum_out need summary_mode 0");
+    const uintptr_t kb = static_cast<uintptr_t>(seg->S) * seg->L * seg->H * 4 * seg->d * 4;
+    if (ksum_in != nullptr && ksum_out != nullptr) {
+      const uintptr_t i0 = reinterpret_cast<uintptr_t>(ksum_in);
+      const uintptr_t o0 = reinterpret_cast<uintptr_t>(ksum_out);
+      if (i0 < o0 + kb && o0 < i0 + kb)
+        return fail(KVC_ERR_ALIAS, "ksum_in and ksum_out overlap");
+    }
+    if ((reinterpret_cast<uintptr_t>(ksum_in) & 3u) || (reinterpret_cast<uintptr_t>(ksum_out) & 3u))
+      return fail(KVC_ERR_ALIGNMENT, "ksum_in / ksum_out must be 4-byte aligned");
+  }
   const size_t need = kvc_chain_edge_workspace(seg, prm);
   if (need > 0) {
     if (workspace == nullptr || workspace_bytes < need)
@@ -605,16 +630,26 @@ kvc_status kvc_chain_edge(int32_t edge, const kvc_segments* seg, const kvc_param
                          best, stream);
   } else {
     e = launch_match(dm, tab, seg->dtype, to_view(ref_K), summaries, prm->top_k,
-                     prm->temperature, weights, best, nullptr, dev_status, stream);
+                     prm->temperature, weights, best, nullptr, dev_status, stream, ksum_in);
   }
   if (e != cudaSuccess) return cuda_fail(e, "kvc_chain_edge match launch");
+  // bf16: the apply epilogue and the fallback copy produce the key sums
+  const bool fused_ksum = ksum_out != nullptr && seg->dtype == KVC_BF16;
   KVC_TRY(apply_impl(seg, prm, tab, ref_K, ref_V, U_K, W_K, U_V, W_V, weights, out_K, out_V,
-                     partial, score, fallback, dev_status, stream));
+                     partial, score, fallback, dev_status, stream,
+                     fused_ksum ? ksum_out : nullptr));
   if (have_dense) {
     const View dv[2] = {to_view(dense_K), to_view(dense_V)};
     const View ov[2] = {to_view(out_K), to_view(out_V)};
-    e = launch_fallback_copy(dm, tab, seg->dtype, dv, ov, fallback, stream);
+    e = launch_fallback_copy(dm, tab, seg->dtype, dv, ov, fallback, stream,
+                             fused_ksum ? ksum_out : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "kvc_chain_edge fallback copy launch");
+  }
+  if (ksum_out != nullptr && !fused_ksum) {
+    // f32: one pass over the held keys this edge leaves
+    e = launch_match(dm, tab, seg->dtype, to_view(out_K), nullptr, prm->top_k, prm->temperature,
+                     nullptr, nullptr, nullptr, dev_status, stream, nullptr, ksum_out);
+    if (e != cudaSuccess) return cuda_fail(e, "kvc_chain_edge key-sum launch");
   }
   return KVC_OK;
 }

@@ -60,15 +60,21 @@ cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t r
 
 // ---------------------------------------------------------------- launchers
 // K2: mean-pooled query, cosine similarities, top-k softmax weights.
+// ksum_in (optional, [units, 4, d]): column sums of the keys from the
+// previous edge, used instead of reading refK; ksum_out (optional): write the
+// column sums of refK as [unit, 0, :] with the other three quadrants zero.
+// summaries == nullptr computes only query / ksum_out.
 cudaError_t launch_match(const Dims& dm, const SegTable& seg, kvc_dtype dtype, const View& refK,
                          const float* summaries, int top_k, float temperature, float* weights,
-                         int32_t* best, float* query, int32_t* dev_status, cudaStream_t stream);
+                         int32_t* best, float* query, int32_t* dev_status, cudaStream_t stream,
+                         const float* ksum_in = nullptr, float* ksum_out = nullptr);
 
-// K3 (bf16, tcgen05): fused correction apply + per-unit norms.
+// K3 (bf16, tcgen05): fused correction apply + per-unit norms; optionally the
+// column sums of the K output rows per TMEM quadrant (ksum [units, 4, d]).
 cudaError_t launch_apply_tc(const Dims& dm, const SegTable& seg, const View refv[2],
                             const View outv[2], const void* U[2], const void* W[2],
-                            const float* weights, float* partial, int32_t* dev_status,
-                            cudaStream_t stream);
+                            const float* weights, float* partial, float* ksum,
+                            int32_t* dev_status, cudaStream_t stream);
 
 // K3 (f32, FP32 FMA): fused correction apply + per-unit norms.
 cudaError_t launch_apply_simt(const Dims& dm, const SegTable& seg, const View refv[2],
@@ -83,10 +89,13 @@ cudaError_t launch_segment_reduce(const Dims& dm, const float* partial, float ta
 cudaError_t launch_select_ratio(const Dims& dm, const float* score, int n_reuse,
                                 uint8_t* fallback, cudaStream_t stream);
 
-// Bit-exact copy of the dense rows of every flagged segment into out.
+// Bit-exact copy of the dense rows of every flagged segment into out; for
+// bf16 with ksum != nullptr also the column sums of the copied K rows
+// (ksum[unit, 0, :], quadrants 1-3 zeroed) of those segments.
 cudaError_t launch_fallback_copy(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
                                  const View densev[2], const View outv[2],
-                                 const uint8_t* fallback, cudaStream_t stream);
+                                 const uint8_t* fallback, cudaStream_t stream,
+                                 float* ksum = nullptr);
 
 // K1: randomized low-rank delta states.
 size_t build_workspace_bytes(const Dims& dm, int l);

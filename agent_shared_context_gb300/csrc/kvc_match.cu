@@ -30,6 +30,8 @@ struct MatchArgs {
   float* weights;                 // [S, L, H, A]
   int32_t* best;                  // [S, L, H]
   float* query;                   // [S, L, H, d] or nullptr
+  const float* ksum_in;           // [S, L, H, 4, d] key column sums (replaces the row pass) or nullptr
+  float* ksum_out;                // [S, L, H, 4, d] written from the row pass, or nullptr
   int32_t L, H, d, A, top_k;
   float inv_temperature;
 };
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(kMatchThreads)
   const int64_t row_bytes = a.s_tok * static_cast<int64_t>(sizeof(T));
 
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  if (g < ng) {
+  if (a.ksum_in == nullptr && g < ng) {
     const char* p = base + static_cast<int64_t>(c) * 16;
     int t = g;
     // four independent 16-byte loads in flight per thread, consumed in row order
@@ -123,21 +125,34 @@ __global__ void __launch_bounds__(kMatchThreads)
     for (int i = 0; i < VEC; ++i) msm[g * a.d + c * VEC + i] = acc[i];
   }
   __syncthreads();
-  // fixed-order sum over row groups -> mean
+  // fixed-order sum over row groups (or over the four given partial sums) -> mean
   const float inv_n = 1.0f / static_cast<float>(n);
   float* q = msm + ng * a.d;
+  const int64_t uoff = static_cast<int64_t>(unit);
   for (int j = tid; j < a.d; j += kMatchThreads) {
     float v = 0.0f;
-    for (int gg = 0; gg < ng; ++gg) v += msm[gg * a.d + j];
+    if (a.ksum_in != nullptr) {
+      const float* p = a.ksum_in + uoff * 4 * a.d + j;
+      v = ((__ldg(p) + __ldg(p + a.d)) + __ldg(p + 2 * a.d)) + __ldg(p + 3 * a.d);
+    } else {
+      for (int gg = 0; gg < ng; ++gg) v += msm[gg * a.d + j];
+      if (a.ksum_out != nullptr) {
+        float* o = a.ksum_out + uoff * 4 * a.d + j;
+        o[0] = v;
+        o[a.d] = 0.0f;
+        o[2 * a.d] = 0.0f;
+        o[3 * a.d] = 0.0f;
+      }
+    }
     q[j] = v * inv_n;
   }
   __syncthreads();
 
   const int warp = tid >> 5, lane = tid & 31;
-  const int64_t uoff = static_cast<int64_t>(unit);
   if (a.query != nullptr) {
     for (int j = tid; j < a.d; j += kMatchThreads) a.query[uoff * a.d + j] = q[j];
   }
+  if (a.summaries == nullptr) return;   // sums / query only
   // |q|^2 by warp 0 (fixed order)
   __shared__ float qq_sh;
   if (warp == 0) {
@@ -275,9 +290,12 @@ cudaError_t launch_match_rep(const Dims& dm, const float* query_rep, const float
 
 cudaError_t launch_match(const Dims& dm, const SegTable& seg, kvc_dtype dtype, const View& refK,
                          const float* summaries, int top_k, float temperature, float* weights,
-                         int32_t* best, float* query, int32_t* dev_status, cudaStream_t stream) {
+                         int32_t* best, float* query, int32_t* dev_status, cudaStream_t stream,
+                         const float* ksum_in, float* ksum_out) {
   (void)dev_status;
   MatchArgs a{};
+  a.ksum_in = ksum_in;
+  a.ksum_out = ksum_out;
   a.ref = static_cast<const char*>(refK.base);
   a.s_req = refK.s_req;
   a.s_layer = refK.s_layer;

@@ -60,7 +60,8 @@ extern "C" kvc_status kvc_chain_edge_noalloc(
     kvc_cache_view ref_V, const float* summaries, const void* U_K, const void* W_K,
     const void* U_V, const void* W_V, kvc_cache_view dense_K, kvc_cache_view dense_V,
     kvc_cache_view out_K, kvc_cache_view out_V, float* weights, int32_t* best, float* score,
-    uint8_t* fallback, int32_t* dev_status, cudaStream_t stream) {
+    uint8_t* fallback, const float* ksum_in, float* ksum_out, int32_t* dev_status,
+    cudaStream_t stream) {
   if (seg != nullptr && seg->S > 0 && seg->L > 0 && seg->H > 0) {
     const long long units = static_cast<long long>(seg->S) * seg->L * seg->H;
     if (units > KVC_NOALLOC_MAX_UNITS) {
@@ -81,6 +82,7 @@ extern "C" kvc_status kvc_chain_edge_noalloc(
     return kvc::set_last_error(KVC_ERR_CUDA, msg);
   }
   return kvc_chain_edge(edge, seg, prm, ref_K, ref_V, summaries, U_K, W_K, U_V, W_V, dense_K,
-                        dense_V, out_K, out_V, weights, best, score, fallback, scratch,
+                        dense_V, out_K, out_V, weights, best, score, fallback, ksum_in,
+                        ksum_out, scratch,
                         kvc::kNoallocFloats * sizeof(float), dev_status, stream);
 }

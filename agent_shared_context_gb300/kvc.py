@@ -105,17 +105,17 @@ lib.kvc_match_anchors.restype = _ST
 lib.kvc_match_anchors.argtypes = [_SEG_P, _PRM_P, _VIEW, _VP, _VP, _VP, _VP, _VP, _VP]
 lib.kvc_apply_correction.restype = _ST
 lib.kvc_apply_correction.argtypes = [_SEG_P, _PRM_P, _VIEW, _VIEW, _VP, _VP, _VP, _VP, _VP,
-                                     _VIEW, _VIEW, _VP, _VP, _VP, _VP, _VP]
+                                     _VIEW, _VIEW, _VP, _VP, _VP, _VP, _VP, _VP]
 lib.kvc_chain_edge_workspace.restype = ctypes.c_size_t
 lib.kvc_chain_edge_workspace.argtypes = [_SEG_P, _PRM_P]
 lib.kvc_chain_edge.restype = _ST
 lib.kvc_chain_edge.argtypes = [ctypes.c_int32, _SEG_P, _PRM_P, _VIEW, _VIEW, _VP, _VP, _VP, _VP,
-                               _VP, _VIEW, _VIEW, _VIEW, _VIEW, _VP, _VP, _VP, _VP, _VP,
+                               _VP, _VIEW, _VIEW, _VIEW, _VIEW, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                ctypes.c_size_t, _VP, _VP]
 lib.kvc_chain_edge_noalloc.restype = _ST
 lib.kvc_chain_edge_noalloc.argtypes = [ctypes.c_int32, _SEG_P, _PRM_P, _VIEW, _VIEW, _VP, _VP, _VP,
                                        _VP, _VP, _VIEW, _VIEW, _VIEW, _VIEW, _VP, _VP, _VP, _VP,
-                                       _VP, _VP]
+                                       _VP, _VP, _VP, _VP]
 lib.kvc_build_representation.restype = _ST
 lib.kvc_build_representation.argtypes = [_SEG_P, _PRM_P, _VIEW, _VP, _VP, _VP, _VP, _VP]
 lib.kvc_match_representation.restype = _ST
@@ -300,11 +300,11 @@ def kvc_match_representation(seg: Segments, prm: kvc_params, query_rep: Ptr, anc
 def kvc_apply_correction(seg: Segments, prm: kvc_params, ref_K, ref_V, U_K: Ptr, W_K: Ptr,
                          U_V: Ptr, W_V: Ptr, weights: Ptr, out_K, out_V, partial: Ptr,
                          score: Ptr, fallback: Ptr, dev_status: Ptr, stream=None,
-                         check: bool = True) -> int:
+                         check: bool = True, ksum_out: Ptr = None) -> int:
     st = lib.kvc_apply_correction(seg.ref, ctypes.byref(prm), _v(ref_K), _v(ref_V), _addr(U_K),
                                   _addr(W_K), _addr(U_V), _addr(W_V), _addr(weights), _v(out_K),
                                   _v(out_V), _addr(partial), _addr(score), _addr(fallback),
-                                  _addr(dev_status), _stream(stream))
+                                  _addr(ksum_out), _addr(dev_status), _stream(stream))
     return _done(st, "kvc_apply_correction", check)
 
 
@@ -312,20 +312,25 @@ def kvc_chain_edge(edge: int, seg: Segments, prm: kvc_params, ref_K, ref_V, summ
                    U_K: Ptr, W_K: Ptr, U_V: Ptr, W_V: Ptr, dense_K, dense_V, out_K, out_V,
                    weights: Ptr, best: Ptr, score: Ptr, fallback: Ptr, workspace: Ptr,
                    dev_status: Ptr, stream=None, workspace_bytes: Optional[int] = None,
-                   check: bool = True) -> int:
+                   check: bool = True, ksum_in: Ptr = None, ksum_out: Ptr = None) -> int:
+    """``ksum_out`` [S, L, H, 4, d] receives the column sums of the held keys
+    this edge leaves; passing it as the next edge's ``ksum_in`` spares that
+    edge's match the pass over the key rows."""
     ws_bytes = _nbytes(workspace) if workspace_bytes is None else int(workspace_bytes)
     st = lib.kvc_chain_edge(int(edge), seg.ref, ctypes.byref(prm), _v(ref_K), _v(ref_V),
                             _addr(summaries), _addr(U_K), _addr(W_K), _addr(U_V), _addr(W_V),
                             _v(dense_K), _v(dense_V), _v(out_K), _v(out_V), _addr(weights),
-                            _addr(best), _addr(score), _addr(fallback), _addr(workspace),
-                            ws_bytes, _addr(dev_status), _stream(stream))
+                            _addr(best), _addr(score), _addr(fallback), _addr(ksum_in),
+                            _addr(ksum_out), _addr(workspace), ws_bytes, _addr(dev_status),
+                            _stream(stream))
     return _done(st, "kvc_chain_edge", check)
 
 
 def kvc_chain_edge_noalloc(edge: int, seg: Segments, prm: kvc_params, ref_K, ref_V,
                            summaries: Ptr, U_K: Ptr, W_K: Ptr, U_V: Ptr, W_V: Ptr, dense_K,
                            dense_V, out_K, out_V, weights: Ptr, best: Ptr, score: Ptr,
-                           fallback: Ptr, dev_status: Ptr, stream=None, check: bool = True) -> int:
+                           fallback: Ptr, dev_status: Ptr, stream=None, check: bool = True,
+                           ksum_in: Ptr = None, ksum_out: Ptr = None) -> int:
     """kvc_chain_edge without a workspace argument, for callers that cannot
     allocate device memory (the library's own device scratch array is used;
     include/kvc.h states its size limit and the rule that overlapping calls
@@ -334,7 +339,8 @@ def kvc_chain_edge_noalloc(edge: int, seg: Segments, prm: kvc_params, ref_K, ref
                                     _addr(summaries), _addr(U_K), _addr(W_K), _addr(U_V),
                                     _addr(W_V), _v(dense_K), _v(dense_V), _v(out_K), _v(out_V),
                                     _addr(weights), _addr(best), _addr(score), _addr(fallback),
-                                    _addr(dev_status), _stream(stream))
+                                    _addr(ksum_in), _addr(ksum_out), _addr(dev_status),
+                                    _stream(stream))
     return _done(st, "kvc_chain_edge_noalloc", check)
 
 

@@ -223,6 +223,30 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- replicas (N > 1)
+def rank_workload(wl, rank: int, world: int):
+    """Weak scaling: every rank corrects its own independent batch of the same
+    shape (seed offset by rank); no data crosses ranks."""
+    import dataclasses
+    return wl if world == 1 else dataclasses.replace(wl, seed=wl.seed + 1000 * rank)
+
+
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The job's time is the slowest rank's (all_reduce MAX of one float)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(tokens_per_step_per_rank: int, world: int, ms_step: float) -> float:
+    """Tokens/s of all ranks together: every rank processed its own batch in
+    (at most) the slowest rank's time."""
+    return tokens_per_step_per_rank * world / (ms_step / 1000.0)
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_kvc(args, wl):
     import torch
@@ -241,8 +265,7 @@ def run_kvc(args, wl):
     dev = torch.device("cuda", local)
 
     # every rank corrects its own independent batch (weak scaling)
-    import dataclasses
-    wl_rank = wl if world == 1 else dataclasses.replace(wl, seed=wl.seed + 1000 * rank)
+    wl_rank = rank_workload(wl, rank, world)
     inp = synth.generate(wl_rank, device=dev)
     runner = ChainRunner(wl_rank, inp, device=dev, use_dense=True)
     stream = torch.cuda.current_stream(dev)
@@ -270,13 +293,10 @@ def run_kvc(args, wl):
     ms = start.elapsed_time(stop)
     if int(runner.dev_status.item()) != 0:
         raise RuntimeError("device status %d" % int(runner.dev_status.item()))
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     ms_step = ms / args.steps
     tokens_step = wl.ph_tokens * wl.edges
-    value = tokens_step * world / (ms_step / 1000.0)
+    value = whole_job_value(tokens_step, world, ms_step)
     clk = clocks.summary()
 
     # ---- dominant kernel: fused correction apply, timed alone with events
@@ -284,6 +304,8 @@ def run_kvc(args, wl):
     seg, prm = runner.seg, runner.prm
     eo = runner.edges[1]
     part = torch.empty((wl.S, wl.L, wl.H, 4), device=dev)
+    # as inside the chain: the apply also hands the next edge its key sums
+    ksum = torch.empty((wl.S, wl.L, wl.H, 4, wl.d), device=dev) if runner.carry_ksum else None
     n_rep = 10
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n_rep)]
@@ -292,7 +314,7 @@ def run_kvc(args, wl):
             evs[i - 2][0].record(stream)
         kvc.kvc_apply_correction(seg, prm, inp.exact_K[0], inp.exact_V[0], e.U_K, e.W_K, e.U_V,
                                  e.W_V, eo.weights, eo.out_K, eo.out_V, part, eo.score,
-                                 eo.fallback, runner.dev_status)
+                                 eo.fallback, runner.dev_status, ksum_out=ksum)
         if i >= 2:
             evs[i - 2][1].record(stream)
     torch.cuda.synchronize(dev)

@@ -101,7 +101,7 @@ extern "C" {
 #endif
 
 #define KVC_VERSION_MAJOR 0
-#define KVC_VERSION_MINOR 2
+#define KVC_VERSION_MINOR 3
 
 typedef enum kvc_status {
   KVC_OK = 0,
@@ -280,7 +280,8 @@ kvc_status kvc_match_representation(const kvc_segments* seg, const kvc_params* p
  * then score[s] and fallback[s] = score[s] > tau.  Only PH rows of out are
  * written.  out_K/out_V may not overlap ref_K/ref_V.  bf16 runs on tcgen05
  * tensor cores (weights folded into W in bf16, fp32 accumulation, RNE
- * rounding of out); f32 runs on FP32 FMA.
+ * rounding of out); f32 runs on FP32 FMA.  ksum_out (may be NULL) receives the
+ * column sums of the corrected out_K rows in the kvc_chain_edge layout.
  * ------------------------------------------------------------------------- */
 kvc_status kvc_apply_correction(const kvc_segments* seg, const kvc_params* prm,
                                 kvc_cache_view ref_K, kvc_cache_view ref_V,
@@ -289,7 +290,7 @@ kvc_status kvc_apply_correction(const kvc_segments* seg, const kvc_params* prm,
                                 const float* weights,
                                 kvc_cache_view out_K, kvc_cache_view out_V,
                                 float* partial, float* score, uint8_t* fallback,
-                                int32_t* dev_status, cudaStream_t stream);
+                                float* ksum_out, int32_t* dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * kvc_chain_edge -- one workflow edge of the chained correction (listing,
@@ -309,6 +310,18 @@ kvc_status kvc_apply_correction(const kvc_segments* seg, const kvc_params* prm,
  *   PH segments are not touched.  `workspace` must hold
  *   kvc_chain_edge_workspace() bytes (per-unit norms, and the query
  *   representations in summary_mode 1), 256-byte aligned.
+ *
+ * Key sums carried along the chain (summary_mode 0 only; both may be NULL):
+ *   ksum_out  [S, L, H, 4, d] float32: the column sums of out_K over each
+ *             segment's rows as this edge leaves them (corrected rows, or
+ *             the dense rows of a flagged segment), as four partial sums
+ *             whose total in index order is the column sum.  For bf16 the
+ *             apply kernel and the fallback copy produce them on the fly;
+ *             for f32 one extra pass reads out_K.
+ *   ksum_in   the ksum_out of the edge that produced ref_K: the match then
+ *             reads these 4 * d floats per unit instead of the segment's
+ *             key rows.  The caller guarantees they describe ref_K.
+ *   The two may not overlap.  In summary_mode 1 both must be NULL.
  * ------------------------------------------------------------------------- */
 size_t kvc_chain_edge_workspace(const kvc_segments* seg, const kvc_params* prm);
 kvc_status kvc_chain_edge(int32_t edge, const kvc_segments* seg, const kvc_params* prm,
@@ -319,6 +332,7 @@ kvc_status kvc_chain_edge(int32_t edge, const kvc_segments* seg, const kvc_param
                           kvc_cache_view dense_K, kvc_cache_view dense_V,
                           kvc_cache_view out_K, kvc_cache_view out_V,
                           float* weights, int32_t* best, float* score, uint8_t* fallback,
+                          const float* ksum_in, float* ksum_out,
                           void* workspace, size_t workspace_bytes,
                           int32_t* dev_status, cudaStream_t stream);
 
@@ -338,7 +352,9 @@ kvc_status kvc_chain_edge(int32_t edge, const kvc_segments* seg, const kvc_param
  *
  * Limits and rules:
  *   - S * L * H must not exceed KVC_NOALLOC_MAX_UNITS, else the call returns
- *     KVC_ERR_WORKSPACE with a message, before anything is launched;
+ *     KVC_ERR_WORKSPACE with a message, before anything is launched; in
+ *     summary_mode 1 the query representations must fit as well (d * r_C
+ *     more floats per unit), else KVC_ERR_WORKSPACE;
  *   - the first call on a device (any edge) looks up the array's device
  *     address for that device; make that first call before any stream
  *     capture;
@@ -356,6 +372,7 @@ kvc_status kvc_chain_edge_noalloc(int32_t edge, const kvc_segments* seg, const k
                                   kvc_cache_view dense_K, kvc_cache_view dense_V,
                                   kvc_cache_view out_K, kvc_cache_view out_V,
                                   float* weights, int32_t* best, float* score, uint8_t* fallback,
+                                  const float* ksum_in, float* ksum_out,
                                   int32_t* dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------

@@ -305,3 +305,15 @@ def test_chain_edge_workspace_in_representation_mode():
     assert _chain(a, 1, need - 1, prm=prm) == kvc.KVC_ERR_WORKSPACE
     assert _chain(a, 1, need, prm=_rep_prm(omega_c=None)) == kvc.KVC_ERR_INVALID_ARGUMENT
     assert _chain(a, 1, need, prm=prm, summaries=FAKE + 4) == kvc.KVC_ERR_ALIGNMENT
+
+
+def test_chain_edge_ksum_validation():
+    a = Args()
+    need = kvc.kvc_chain_edge_workspace(a.seg, a.prm)
+    kb = 2 * 2 * 2 * 4 * 128 * 4
+    assert _chain(a, 1, need, ksum_in=FAKE + (1 << 40), ksum_out=FAKE + (1 << 40) + kb - 4) == kvc.KVC_ERR_ALIAS
+    assert _chain(a, 1, need, ksum_out=FAKE + (1 << 40) + 2) == kvc.KVC_ERR_ALIGNMENT
+    prm = _rep_prm()
+    need_r = kvc.kvc_chain_edge_workspace(a.seg, prm)
+    assert _chain(a, 1, need_r, prm=prm, ksum_out=FAKE + (1 << 40)) == kvc.KVC_ERR_INVALID_ARGUMENT
+    assert "summary_mode 0" in kvc.lib.kvc_last_error().decode()
