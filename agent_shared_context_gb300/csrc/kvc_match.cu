@@ -211,6 +211,40 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
+// Sum over the 2 x 2 blocks of the r_C x r_C products X^T Y (and, with
+// Y == nullptr, X^T X) of their squared entries; each thread owns whole 2 x 2
+// blocks (float2 loads of two adjacent columns, 8 FMAs per row c).
+__device__ __forceinline__ void gram_sq(const float* X, const float* Y, int d, int rc, float& sxy,
+                                        float& syy) {
+  const int hb = (rc + 1) >> 1;                    // 2-column blocks per side
+  sxy = 0.0f;
+  syy = 0.0f;
+  for (int e = threadIdx.x; e < hb * hb; e += kMatchThreads) {
+    const int bi = e / hb, bj = e - (e / hb) * hb;
+    const int i0 = 2 * bi, j0 = 2 * bj;
+    const bool i1 = i0 + 1 < rc, j1 = j0 + 1 < rc;
+    float g00 = 0.0f, g01 = 0.0f, g10 = 0.0f, g11 = 0.0f;   // X^T Y
+    float h00 = 0.0f, h01 = 0.0f, h10 = 0.0f, h11 = 0.0f;   // Y^T Y
+    for (int c = 0; c < d; ++c) {
+      const float* xr = X + c * rc;
+      const float* yr = Y + c * rc;
+      const float x0 = xr[i0], x1 = i1 ? xr[i0 + 1] : 0.0f;
+      const float yi0 = yr[i0], yi1 = i1 ? yr[i0 + 1] : 0.0f;
+      const float y0 = yr[j0], y1 = j1 ? yr[j0 + 1] : 0.0f;
+      g00 = fmaf(x0, y0, g00);
+      g01 = fmaf(x0, y1, g01);
+      g10 = fmaf(x1, y0, g10);
+      g11 = fmaf(x1, y1, g11);
+      h00 = fmaf(yi0, y0, h00);
+      h01 = fmaf(yi0, y1, h01);
+      h10 = fmaf(yi1, y0, h10);
+      h11 = fmaf(yi1, y1, h11);
+    }
+    sxy += (g00 * g00 + g01 * g01) + (g10 * g10 + g11 * g11);
+    syy += (h00 * h00 + h01 * h01) + (h10 * h10 + h11 * h11);
+  }
+}
+
 __global__ void __launch_bounds__(kMatchThreads) match_rep_kernel(const MatchRepArgs a) {
   extern __shared__ float4 rsm4[];
   float* Rq = reinterpret_cast<float*>(rsm4);      // [d][rc]
@@ -220,37 +254,21 @@ __global__ void __launch_bounds__(kMatchThreads) match_rep_kernel(const MatchRep
   __shared__ float red[kMatchThreads / 32];
   const int tid = threadIdx.x;
   const int64_t unit = blockIdx.x;
-  const int rc = a.rc, d = a.d, ne = rc * rc;
 
   const float4* q4 = reinterpret_cast<const float4*>(a.query + unit * n);
   for (int i = tid; i < n / 4; i += kMatchThreads) rsm4[i] = __ldg(q4 + i);
   __syncthreads();
-  // |Rq^T Rq|_F^2: thread handles Gram entries e = tid, tid + 256, ...
-  float v = 0.0f;
-  for (int e = tid; e < ne; e += kMatchThreads) {
-    const int i = e / rc, j = e - (e / rc) * rc;
-    float g = 0.0f;
-    for (int c = 0; c < d; ++c) g = fmaf(Rq[c * rc + i], Rq[c * rc + j], g);
-    v = fmaf(g, g, v);
-  }
-  const float gqq = block_sum(v, red);
+  // |Rq^T Rq|_F^2
+  float vqq, unused;
+  gram_sq(Rq, Rq, a.d, a.rc, unused, vqq);
+  const float gqq = block_sum(vqq, red);
   for (int an = 0; an < a.A; ++an) {
     const float4* a4 = reinterpret_cast<const float4*>(a.anchors + (unit * a.A + an) * n);
     float4* ra4 = reinterpret_cast<float4*>(Ra);
     for (int i = tid; i < n / 4; i += kMatchThreads) ra4[i] = __ldg(a4 + i);
     __syncthreads();
-    float vqa = 0.0f, vaa = 0.0f;
-    for (int e = tid; e < ne; e += kMatchThreads) {
-      const int i = e / rc, j = e - (e / rc) * rc;
-      float gqa = 0.0f, gaa = 0.0f;
-      for (int c = 0; c < d; ++c) {
-        const float raj = Ra[c * rc + j];
-        gqa = fmaf(Rq[c * rc + i], raj, gqa);
-        gaa = fmaf(Ra[c * rc + i], raj, gaa);
-      }
-      vqa = fmaf(gqa, gqa, vqa);
-      vaa = fmaf(gaa, gaa, vaa);
-    }
+    float vqa, vaa;
+    gram_sq(Rq, Ra, a.d, a.rc, vqa, vaa);            // |Rq^T Ra|^2 and |Ra^T Ra|^2
     const float sqa = block_sum(vqa, red);
     const float saa = block_sum(vaa, red);
     if (tid == 0)

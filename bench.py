@@ -442,10 +442,31 @@ def _e2e(args, wl, inp, runner, dev):
     d2h = sum(h.numel() * h.element_size() for h in host_out)
     stream = torch.cuda.current_stream(dev)
     steps = max(1, args.e2e_steps)
+    # the uploads are spread over several copy streams (largest first, to the
+    # least loaded stream) so that more than one copy engine moves data; the
+    # compute stream waits for all of them
+    n_copy = 4
+    copy_streams = [torch.cuda.Stream(dev) for _ in range(n_copy)]
+    order = sorted(range(len(host_in)), key=lambda i: -host_in[i].numel() * host_in[i].element_size())
+    load = [0] * n_copy
+    assign = {}
+    for i in order:
+        k = min(range(n_copy), key=lambda c: load[c])
+        assign[i] = k
+        load[k] += host_in[i].numel() * host_in[i].element_size()
 
     def step():
-        for h, d in zip(host_in, dev_in):
-            d.copy_(h, non_blocking=True)
+        ready = torch.cuda.Event()
+        ready.record(stream)                     # the previous step's kernels are done with the inputs
+        for cs in copy_streams:
+            cs.wait_event(ready)
+        for i, (h, d) in enumerate(zip(host_in, dev_in)):
+            with torch.cuda.stream(copy_streams[assign[i]]):
+                d.copy_(h, non_blocking=True)
+        for cs in copy_streams:
+            done = torch.cuda.Event()
+            done.record(cs)
+            stream.wait_event(done)
         runner.run()
         for h, d in zip(host_out, outs):
             h.copy_(d, non_blocking=True)
