@@ -80,6 +80,29 @@ def _peaks():
         return HBM_FALLBACK_GBS, "fallback"
 
 
+def _bf16_peak():
+    """Dense bf16 TFLOP/s (burst, for a kernel timed alone)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def _time_launches(torch, stream, fn, n: int = 20, warm: int = 2) -> float:
+    """Mean CUDA-event duration (ms) of n back-to-back calls of fn on stream."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for i in range(n + warm):
+        if i >= warm:
+            evs[i - warm][0].record(stream)
+        fn()
+        if i >= warm:
+            evs[i - warm][1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
 def _profile_traffic(workload: str):
     """DRAM bytes per launch of the apply kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -329,6 +352,24 @@ def run_kvc(args, wl):
     achieved = apply_bytes / (apply_ms / 1000.0) / 1e9
     traffic = _profile_traffic(wl.name)
 
+    # ---- match alone (mean keys: the K_ref read) and one whole edge
+    match = None
+    edge = None
+    match_bytes = wl.ph_tokens * wl.L * wl.H * wl.d * ebytes + wl.S * wl.L * wl.H * wl.A * (wl.d + 1) * 4
+    if not runner.rank_mode:
+        m_ms = _time_launches(torch, stream, lambda: kvc.kvc_match_anchors(
+            seg, prm, inp.exact_K[0], e.summaries, eo.weights, eo.best, None, runner.dev_status))
+        m_gbs = match_bytes / (m_ms / 1000.0) / 1e9
+        match = {"kernel": "match_kernel", "launch_ms": m_ms, "algorithmic_bytes_per_launch": match_bytes,
+                 "achieved": m_gbs, "peak": peak, "unit": "GB/s", "frac": m_gbs / peak}
+    e_ms = _time_launches(torch, stream, lambda: runner.run_edge(1), n=10)
+    e_bytes = apply_bytes + (0 if runner.rank_mode else match_bytes)
+    edge = {"what": "edge 1 through kvc_chain_edge (match from the keys, apply, reduce, fallback copy)"
+                    + (" after the state build" if runner.build else ""),
+            "ms": e_ms, "tokens_per_s": wl.ph_tokens / (e_ms / 1000.0),
+            "apply_plus_match_bytes": e_bytes,
+            "frac_of_peak_over_apply_plus_match_bytes": e_bytes / (e_ms / 1000.0) / 1e9 / peak}
+
     # ---- state builder (workloads that build anchor states), timed alone
     builder = None
     if runner.build:
@@ -351,9 +392,19 @@ def run_kvc(args, wl):
         for s in range(wl.S):
             gemm_flop += wl.L * wl.H * 2 * 2 * (2 * wl.power_iters + 2) * wl.seg_len[s] * wl.d * wl.l
         tc = wl.d <= 128 and wl.l <= 64
+        # bytes the builder must move: exact and held rows read, U and W written
+        b_bytes = sum(wl.L * wl.H * 2 * (2 * n * wl.d * ebytes + (n + wl.d) * wl.r * ebytes)
+                      for n in wl.seg_len)
+        bf16_pk, bf16_kind = _bf16_peak()
+        tflops = gemm_flop / (b_ms / 1000.0) / 1e12
+        b_gbs = b_bytes / (b_ms / 1000.0) / 1e9
         builder = {"kernel": "build_tc_kernel" if tc else "build_simt_kernel",
                    "launch_ms": b_ms, "matrices": mats,
-                   "hmt_gemm_equivalent_tflops": gemm_flop / (b_ms / 1000.0) / 1e12,
+                   "hmt_gemm_equivalent_tflops": tflops,
+                   "tensor_frac_of_bf16_peak": tflops / bf16_pk, "bf16_peak_tflops": bf16_pk,
+                   "bf16_peak_kind": bf16_kind,
+                   "algorithmic_bytes": b_bytes, "achieved_gbs": b_gbs, "hbm_frac": b_gbs / peak,
+                   "bound": "latency of the fp32 small-matrix steps (see profiles)",
                    "tensor_path": ("M = delta^T delta on tcgen05 (split bf16)" if tc
                                    else "FP32 FMA")}
 
@@ -399,8 +450,14 @@ def run_kvc(args, wl):
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
         "builder": builder,
+        "match": match,
+        "edge": edge,
         "e2e": e2e,
     }
+    # analytic bytes of a rank-r state per anchor against a full-dimensional
+    # anchor (T_s x d per K or V), averaged over the segments
+    line["config"]["anchor_bytes_vs_full_dim"] = statistics.mean(
+        (n * wl.d) / (wl.r * (n + wl.d)) for n in wl.seg_len)
     if representation is not None:
         line["representation"] = representation
         line["config"]["summary"] = "rank-%d representations" % wl.rank_c
