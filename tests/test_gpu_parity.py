@@ -57,6 +57,9 @@ def _cases():
                                        pf=3, fallback_frac=0.0),
         # the tiny fp32 workload (FP32 FMA path), anchors as generated
         "tiny-f32": dataclass_replace(synth.workload("tiny"), build_slot=-1),
+        # the largest segment table one call accepts: 4 requests x 256 segments
+        "max-segments": synth.scaled(L2K, L=1, H=1, R=4, seg_len=[24], segs_per_req=256,
+                                     fallback_frac=0.1),
     }
 
 
