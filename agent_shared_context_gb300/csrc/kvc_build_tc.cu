@@ -152,7 +152,8 @@ __device__ void mm(const float* A, int lda, bool transA, const float* B, int ldb
 // whole CTA with one barrier per column.  The trailing update uses the
 // unscaled pivot row (R[i][k] -= R[j][i] R[j][k] / pivot_j) so the rows can
 // be scaled once at the end.  `pairs_ik` lists the (i, k <= l) index pairs of
-// the upper triangle, i in the high byte.  A pivot below 1e-6 of its
+// the upper triangle row by row (i ascending), i in the high byte; step j
+// visits only the rows below it.  A pivot below 1e-6 of its
 // column's squared norm marks a dependent column: keep[j] = 0, row j zero.
 __device__ void chol(const float* G, float* R, int* keep, float* dinv,
                      const uint16_t* pairs_ik, int l, int ls) {
@@ -172,9 +173,12 @@ __device__ void chol(const float* G, float* R, int* keep, float* dinv,
       keep[j] = ok ? 1 : 0;
       dinv[j] = ok ? rsqrtf(piv) : 0.0f;
     }
-    for (int p = threadIdx.x; p < npairs; p += kTcThreads) {
+    // pairs are listed row by row, so the rows i > j start at index
+    // sum_{i <= j} (l - i)
+    const int first = (j + 1) * l - ((j + 1) * j) / 2;
+    for (int p = first + threadIdx.x; p < npairs; p += kTcThreads) {
       const int i = pairs_ik[p] >> 8, k = pairs_ik[p] & 255;
-      if (i > j) R[i * ls + k] = fmaf(-R[j * ls + i] * inv2, R[j * ls + k], R[i * ls + k]);
+      R[i * ls + k] = fmaf(-R[j * ls + i] * inv2, R[j * ls + k], R[i * ls + k]);
     }
     __syncthreads();
   }
@@ -223,7 +227,8 @@ __device__ void tri_inv(const float* R, const int* keep, float* Ri, int l, int l
 // both sides at once, so one barrier suffices) and V' = V J alongside.  A
 // pair is rotated only while |a_pq| > max(1e-7 sqrt(|a_pp a_qq|),
 // 2e-7 max|a_ii|) -- the absolute floor sits above fp32 rounding noise -- and
-// the solver stops after the first sweep that rotates nothing (or kSweeps).
+// the solver stops before the first sweep that would rotate nothing (or after
+// kSweeps).
 __device__ void jacobi(float* A, float* V, int l, int ls, float* cs, int* pairs, float* red,
                        uint16_t* items) {
   const int n = (l + 1) & ~1;
@@ -248,6 +253,17 @@ __device__ void jacobi(float* A, float* V, int l, int ls, float* cs, int* pairs,
     dmax = 0.0f;
     for (int w = 0; w < kTcThreads / 32; ++w) dmax = fmaxf(dmax, red[w]);
     const float abs_tol = 2e-7f * dmax;
+    // A sweep that would rotate no pair leaves A and V unchanged: test every
+    // pair against the rotation criterion below and stop without running it.
+    int active = 0;
+    for (int idx = threadIdx.x; idx < l * l; idx += kTcThreads) {
+      const int p = idx / l, q = idx - (idx / l) * l;
+      if (p < q) {
+        const float apq = A[p * ls + q], app = A[p * ls + p], aqq = A[q * ls + q];
+        if (fabsf(apq) > fmaxf(1e-7f * sqrtf(fabsf(app * aqq)), abs_tol)) active = 1;
+      }
+    }
+    if (!__syncthreads_or(active)) break;
     int rotated = 0;
     for (int round = 0; round < n - 1; ++round) {
       if (threadIdx.x < np) {

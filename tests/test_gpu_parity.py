@@ -346,3 +346,47 @@ def test_reuse_ratio_mode_on_gpu():
         if 0 < k < wl.S and (srt[k - 1] - srt[k]) < 1e-3 * srt[k - 1]:
             continue
         assert np.array_equal(fbg, ofb), (rho, fbg, ofb, osc)
+
+
+def test_chain_without_dense_rows_matches_oracle():
+    """dense_K/dense_V NULL: flagged segments keep their corrected rows (the
+    caller prefills them itself from the returned flags), and those rows are
+    the next edge's reference -- on both sides."""
+    from agent_shared_context_gb300.chain import ChainRunner
+    wl = _cases()["concurrent-small"]
+    inp = synth.generate(wl, device="cuda")
+    runner = ChainRunner(wl, inp, device="cuda", use_dense=False, poison_ph=True)
+    runner.run()
+    torch.cuda.synchronize()
+    assert int(runner.dev_status.item()) == 0
+    res, _ = oracle_chain(wl, inp, use_dense=False)
+    flagged = 0
+    for j in range(1, wl.edges + 1):
+        eo = runner.edges[j]
+        fb = eo.fallback.cpu().numpy().astype(bool)
+        assert np.array_equal(fb, res[j]["fallback"]), j
+        flagged += int(fb.sum())
+        none = np.zeros(wl.S, dtype=bool)                  # every segment holds corrected rows
+        check_out(wl, j, np64(eo.out_K), res[j]["out_K"], res[j - 1]["out_K"], none, True)
+        check_out(wl, j, np64(eo.out_V), res[j]["out_V"], res[j - 1]["out_V"], none, True)
+    assert flagged > 0
+
+
+def test_every_segment_falls_back():
+    """All segments planted above tau: every PH row of every agent is the
+    dense row, bit-exactly, and the key sums handed along come from the copy."""
+    from agent_shared_context_gb300.chain import ChainRunner
+    wl = synth.scaled(synth.workload("llama2k"), L=2, H=2, R=2, seg_len=[200, 130], pf=8,
+                      fallback_frac=1.0)
+    inp = synth.generate(wl, device="cuda")
+    runner = ChainRunner(wl, inp, device="cuda", poison_ph=True)
+    runner.run()
+    torch.cuda.synchronize()
+    assert int(runner.dev_status.item()) == 0
+    res, _ = oracle_chain(wl, inp)
+    for j in range(1, wl.edges + 1):
+        eo = runner.edges[j]
+        assert bool(eo.fallback.bool().all()) and bool(res[j]["fallback"].all())
+        assert torch.equal(eo.out_K, inp.exact_K[j]) and torch.equal(eo.out_V, inp.exact_V[j])
+        np.testing.assert_allclose(eo.weights.cpu().numpy(), res[j]["weights"], rtol=1e-2,
+                                   atol=2e-4)
