@@ -653,50 +653,54 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     T* Uo = reinterpret_cast<T*>(a.U[kv]) + static_cast<int64_t>(unit) * a.Tmax * a.A * r;
     constexpr int VEC = 16 / sizeof(T);                  // elements per 16-byte load
     const bool vec_r = (r & 3) == 0;
+    // rank columns in blocks of 32 (8 float4 accumulators: no spills under
+    // the two-CTA register budget); r <= 32 takes one pass
     for (int t = threadIdx.x; t < a.Tmax; t += kTcThreads) {
       T* urow = Uo + (static_cast<int64_t>(t) * a.A + slot) * r;
-      float4 acc[kLmax / 4];
+      for (int j0 = 0; j0 < r; j0 += 32) {
+        float4 acc[8];
 #pragma unroll
-      for (int q4 = 0; q4 < kLmax / 4; ++q4) acc[q4] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      if (t < n) {
-        for (int c0 = 0; c0 < d; c0 += VEC) {
-          const uint4 xe = *reinterpret_cast<const uint4*>(ex + t * es3 + c0);
-          const uint4 xr = *reinterpret_cast<const uint4*>(rf + t * rs3 + c0);
-          const T* pe = reinterpret_cast<const T*>(&xe);
-          const T* pq = reinterpret_cast<const T*>(&xr);
+        for (int q4 = 0; q4 < 8; ++q4) acc[q4] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (t < n) {
+          for (int c0 = 0; c0 < d; c0 += VEC) {
+            const uint4 xe = *reinterpret_cast<const uint4*>(ex + t * es3 + c0);
+            const uint4 xr = *reinterpret_cast<const uint4*>(rf + t * rs3 + c0);
+            const T* pe = reinterpret_cast<const T*>(&xe);
+            const T* pq = reinterpret_cast<const T*>(&xr);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const float dv = to_f<T>(pe[e]) - to_f<T>(pq[e]);
-            const float* pr = P1 + (c0 + e) * r;
-            if (vec_r) {
+            for (int e = 0; e < VEC; ++e) {
+              const float dv = to_f<T>(pe[e]) - to_f<T>(pq[e]);
+              const float* pr = P1 + (c0 + e) * r + j0;
+              if (vec_r) {
 #pragma unroll
-              for (int q4 = 0; q4 < kLmax / 4; ++q4) {
-                if (4 * q4 < r) {
-                  const float4 pv = *reinterpret_cast<const float4*>(pr + 4 * q4);
-                  acc[q4].x = fmaf(dv, pv.x, acc[q4].x);
-                  acc[q4].y = fmaf(dv, pv.y, acc[q4].y);
-                  acc[q4].z = fmaf(dv, pv.z, acc[q4].z);
-                  acc[q4].w = fmaf(dv, pv.w, acc[q4].w);
+                for (int q4 = 0; q4 < 8; ++q4) {
+                  if (j0 + 4 * q4 < r) {
+                    const float4 pv = *reinterpret_cast<const float4*>(pr + 4 * q4);
+                    acc[q4].x = fmaf(dv, pv.x, acc[q4].x);
+                    acc[q4].y = fmaf(dv, pv.y, acc[q4].y);
+                    acc[q4].z = fmaf(dv, pv.z, acc[q4].z);
+                    acc[q4].w = fmaf(dv, pv.w, acc[q4].w);
+                  }
                 }
-              }
-            } else {
+              } else {
 #pragma unroll
-              for (int q4 = 0; q4 < kLmax / 4; ++q4) {
-                float* av = reinterpret_cast<float*>(&acc[q4]);
+                for (int q4 = 0; q4 < 8; ++q4) {
+                  float* av = reinterpret_cast<float*>(&acc[q4]);
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                  if (4 * q4 + u < r) av[u] = fmaf(dv, pr[4 * q4 + u], av[u]);
+                  for (int u = 0; u < 4; ++u)
+                    if (j0 + 4 * q4 + u < r) av[u] = fmaf(dv, pr[4 * q4 + u], av[u]);
+                }
               }
             }
           }
         }
-      }
 #pragma unroll
-      for (int q4 = 0; q4 < kLmax / 4; ++q4) {
-        const float* av = reinterpret_cast<const float*>(&acc[q4]);
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float* av = reinterpret_cast<const float*>(&acc[q4]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (4 * q4 + u < r) store_out<T>(urow + 4 * q4 + u, av[u]);
+          for (int u = 0; u < 4; ++u)
+            if (j0 + 4 * q4 + u < r) store_out<T>(urow + j0 + 4 * q4 + u, av[u]);
+        }
       }
     }
     // ---- pool insertion: the new anchor's summary is the held key mean
