@@ -14,9 +14,17 @@ Default workload: the Llama-3.1-8B-shaped 2K chain (32 layers x 8 KV heads x
 d 128, bf16, 10 requests x 2,048 shared tokens, 8 anchors, r = 32, tau 0.32,
 10% planted fallback).
 
-Prints ONE JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
-oracle instead (the only other place this file executes the oracle is the
-``cpu_baseline`` leg).
+Prints ONE JSON line on rank 0: the headline metric, the apply kernel's
+roofline (algorithmic bytes over its CUDA-event time against the measured HBM
+copy peak, and the DRAM traffic of the committed ncu capture), clocks sampled
+during the timed region, the end-to-end number with host buffers (``e2e``),
+the oracle's CPU rate (``cpu_baseline``), and the fractions of the other
+steps: ``match`` (the mean-key match alone), ``edge`` (one whole edge),
+``builder`` (workloads that build states) and ``representation``
+(rank-r_C workloads).  Under torchrun every rank corrects its own batch
+(weak scaling); the time is the slowest rank's.  ``--impl reference`` times
+the fp64 CPU oracle instead (the only other place this file executes the
+oracle is the ``cpu_baseline`` leg).
 """
 from __future__ import annotations
 
