@@ -57,6 +57,11 @@ def _cases():
                                        pf=3, fallback_frac=0.0),
         # the tiny fp32 workload (FP32 FMA path), anchors as generated
         "tiny-f32": dataclass_replace(synth.workload("tiny"), build_slot=-1),
+        # the widest anchor set: A = 32 (a full warp of similarities), K = A * r = 512
+        "A32-r16": synth.scaled(L2K, L=1, H=2, R=2, seg_len=[150], A=32, r=16, top_k=5,
+                                fallback_frac=0.5),
+        # the largest rank: r = 64, K = 512
+        "r64-A8": synth.scaled(L2K, L=1, H=2, R=2, seg_len=[140], r=64, top_k=4),
         # the largest segment table one call accepts: 4 requests x 256 segments
         "max-segments": synth.scaled(L2K, L=1, H=1, R=4, seg_len=[24], segs_per_req=256,
                                      fallback_frac=0.1),
