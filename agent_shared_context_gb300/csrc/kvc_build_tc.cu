@@ -498,32 +498,51 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     float ss = 0.0f;
     const int nchunks = (n + kTok - 1) / kTok;
     for (int kc = 0; kc < nchunks; ++kc) {
-      for (int u = threadIdx.x; u < kDP * 8; u += kTcThreads) {
-        const int c = u & (kDP - 1);                  // feature row
-        const int g = u >> 7;                         // 8-token group of the chunk
+      // thread = (EPL adjacent features, 8 tokens): eight 8-byte loads per
+      // operand in flight, then per feature one 16-byte row of hi and of lo
+      // (units fg * 8 + g cover FG feature groups x 8 token groups)
+      constexpr int EPL = 8 / static_cast<int>(sizeof(T));   // elements per 8-byte load
+      constexpr int FG = kDP / EPL;                           // feature groups
+      for (int u = threadIdx.x; u < FG * 8; u += kTcThreads) {
+        // adjacent lanes take adjacent token groups: a warp's 16-byte row
+        // stores then hit 8 distinct swizzle slots in each of 4 rows
+        const int g = u & 7, fg = u >> 3;
+        const int c0 = fg * EPL;
         const int t0 = kc * kTok + g * 8;
-        uint32_t hw[4], lw[4];
+        uint2 xe[8], xr[8];
 #pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          float dv[2];
-#pragma unroll
-          for (int e1 = 0; e1 < 2; ++e1) {
-            const int t = t0 + 2 * e2 + e1;
-            float v = 0.0f;
-            if (c < d && t < n)
-              v = to_f<T>(ex[t * es3 + c]) - (rf != nullptr ? to_f<T>(rf[t * rs3 + c]) : 0.0f);
-            dv[e1] = v;
-            ss = fmaf(v, v, ss);
-          }
-          const __nv_bfloat162 hb = __floats2bfloat162_rn(dv[0], dv[1]);
-          const float2 hf = __bfloat1622float2(hb);
-          const __nv_bfloat162 lb = __floats2bfloat162_rn(dv[0] - hf.x, dv[1] - hf.y);
-          hw[e2] = *reinterpret_cast<const uint32_t*>(&hb);
-          lw[e2] = *reinterpret_cast<const uint32_t*>(&lb);
+        for (int i = 0; i < 8; ++i) {
+          const int t = t0 + i;
+          const bool in = c0 < d && t < n;
+          xe[i] = in ? *reinterpret_cast<const uint2*>(ex + t * es3 + c0) : make_uint2(0u, 0u);
+          xr[i] = (in && rf != nullptr) ? *reinterpret_cast<const uint2*>(rf + t * rs3 + c0)
+                                        : make_uint2(0u, 0u);
         }
-        const int off = c * 128 + ((g ^ (c & 7)) << 4);
-        *reinterpret_cast<uint4*>(hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+#pragma unroll
+        for (int f = 0; f < EPL; ++f) {
+          const int c = c0 + f;
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            float dv[2];
+#pragma unroll
+            for (int e1 = 0; e1 < 2; ++e1) {
+              const int i = 2 * e2 + e1;
+              const float v = to_f<T>(reinterpret_cast<const T*>(&xe[i])[f]) -
+                              to_f<T>(reinterpret_cast<const T*>(&xr[i])[f]);
+              dv[e1] = v;
+              ss = fmaf(v, v, ss);
+            }
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(dv[0], dv[1]);
+            const float2 hf = __bfloat1622float2(hb);
+            const __nv_bfloat162 lb = __floats2bfloat162_rn(dv[0] - hf.x, dv[1] - hf.y);
+            hw[e2] = *reinterpret_cast<const uint32_t*>(&hb);
+            lw[e2] = *reinterpret_cast<const uint32_t*>(&lb);
+          }
+          const int off = c * 128 + ((g ^ (c & 7)) << 4);
+          *reinterpret_cast<uint4*>(hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
       }
       fence_proxy_async_smem();
       __syncthreads();
