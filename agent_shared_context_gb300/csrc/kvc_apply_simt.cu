@@ -1,6 +1,7 @@
 // kvc_apply_simt.cu -- FP32 correction apply (f32 caches), the per-segment
-// reliability reduction (K4), the dense-fallback copy, and the bounded-wait
-// self test.
+// reliability reduction (K4), the reuse-ratio selection, the dense-fallback
+// copy (which, for bf16 with key sums requested, also sums the copied K rows
+// for the next edge's query), and the bounded-wait self test.
 //
 // KVCMAS listing, Figure 1(a)-(b): out = ref + sum_a w_a U_a W_a^T on the PH
 // rows of every unit; the segment is reused when the correction is reliable
