@@ -12,6 +12,14 @@ every edge corrects one fixed context-free reference instead (the
 non-chained variant of Figure 3 / Table 8).  Agent A0's cache is the
 exact one and is never written (edge 0 is a validated no-op).
 
+With ``keep_outputs=False`` the runner holds only two corrected caches and
+alternates between them (edge j writes buffer (j - 1) mod 2 while it reads the
+other one, the held cache of agent j - 1): a chain then needs the exact caches
+of its agents, every edge's anchor inputs and two cache-sized outputs, instead
+of one output per edge.  Only the PH rows of a reused buffer are rewritten;
+its PF rows keep the agent-specific prefix of the agent it was created for,
+which no call of the chain reads.
+
 All arithmetic of the correction path runs in libkvc; this module only
 allocates device memory with torch and passes pointers.
 """
@@ -50,7 +58,8 @@ def ph_row_mask(wl: Workload, device) -> torch.Tensor:
 class ChainRunner:
     def __init__(self, wl: Workload, inp: WorkloadInputs, device="cuda", use_dense: bool = True,
                  poison_ph: bool = False, stream: Optional[torch.cuda.Stream] = None,
-                 build: Optional[bool] = None, fixed_ref=None, carry_ksum: bool = True):
+                 build: Optional[bool] = None, fixed_ref=None, carry_ksum: bool = True,
+                 keep_outputs: bool = True):
         self.wl = wl
         self.inp = inp
         self.device = torch.device(device)
@@ -75,11 +84,16 @@ class ChainRunner:
         bws = kvc.kvc_build_states_workspace(self.seg, self.prm) if self.build else 0
         self.build_ws = torch.empty(max(bws, 256), dtype=torch.uint8, device=dev)
         mask = ph_row_mask(wl, dev)
+        self.keep_outputs = keep_outputs
         self.edges: List[Optional[EdgeOutputs]] = [None]
         for j in range(1, wl.edges + 1):
-            oK = inp.exact_K[j].clone()
-            oV = inp.exact_V[j].clone()
-            if poison_ph:
+            if not keep_outputs and j > 2:
+                # ping-pong: edge j reuses the buffers of edge j - 2
+                oK, oV = self.edges[j - 2].out_K, self.edges[j - 2].out_V
+            else:
+                oK = inp.exact_K[j].clone()
+                oV = inp.exact_V[j].clone()
+            if poison_ph and (keep_outputs or j <= 2):
                 # PH rows start as NaN so any row the library fails to write shows up
                 nan = torch.tensor(float("nan"), dtype=oK.dtype, device=dev)
                 for q in range(wl.R):

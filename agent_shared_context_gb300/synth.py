@@ -310,6 +310,21 @@ class WorkloadInputs:
     context_free_V: Optional[torch.Tensor] = None
     omega_c: Optional[torch.Tensor] = None   # [d, l_C] test matrix of the representations
 
+    def to(self, device) -> "WorkloadInputs":
+        """The same tensors on ``device`` (e.g. generated on the host, then
+        copied to the GPU once)."""
+        def mv(t):
+            return None if t is None else t.to(device)
+
+        edges = [None if e is None else EdgeInputs(
+            U_K=mv(e.U_K), W_K=mv(e.W_K), U_V=mv(e.U_V), W_V=mv(e.W_V),
+            summaries=mv(e.summaries), planted=e.planted, reps=mv(e.reps)) for e in self.edges]
+        return WorkloadInputs(wl=self.wl, exact_K=[mv(t) for t in self.exact_K],
+                              exact_V=[mv(t) for t in self.exact_V], edges=edges,
+                              omega=mv(self.omega), planted_ratio=self.planted_ratio,
+                              context_free_K=mv(self.context_free_K),
+                              context_free_V=mv(self.context_free_V), omega_c=mv(self.omega_c))
+
 
 def _seg_ratio(wl: Workload, planted: bool) -> float:
     """Target ratio |Delta_r|_F / |ref|_F for a unit of a segment.
@@ -320,11 +335,14 @@ def _seg_ratio(wl: Workload, planted: bool) -> float:
     return wl.tau * (1.9 if planted else 0.4)
 
 
-def generate(wl: Workload, device="cpu", edges: Optional[Sequence[int]] = None) -> WorkloadInputs:
+def generate(wl: Workload, device="cpu", edges: Optional[Sequence[int]] = None,
+             context_free: bool = True) -> WorkloadInputs:
     """Generate every agent's exact cache and every edge's anchor inputs.
 
     ``edges`` restricts which edges get anchor inputs (others are None); the
-    exact caches of all agents are always generated (they chain)."""
+    exact caches of all agents are always generated (they chain).  With
+    ``context_free=False`` the context-free reference of the non-chained
+    variant (one more cache-sized tensor pair) is not generated."""
     device = torch.device(device)
     dt = wl.torch_dtype
     R, L, H, T, d = wl.R, wl.L, wl.H, wl.T, wl.d
@@ -438,7 +456,7 @@ def generate(wl: Workload, device="cpu", edges: Optional[Sequence[int]] = None) 
             if j in want:
                 gs = _generator(device, wl, "summary", j, s)
                 kmean = prevK[q, :, :, t0:t0 + n, :].float().mean(dim=2)      # [L, H, d]
-                summ[s] = kmean.unsqueeze(2) + wl.summary_noise * _randn((L, H, A, d), gs, device)
+                summ[s] = _summaries(wl, kmean, gs, device)
                 if reps is not None:
                     reps[s] = _anchor_reps(wl, prevK[q, :, :, t0:t0 + n, :],
                                            _generator(device, wl, "rep", j, s), device)
@@ -451,13 +469,44 @@ def generate(wl: Workload, device="cpu", edges: Optional[Sequence[int]] = None) 
 
     go = _generator(device, wl, "omega")
     omega = _randn((d, wl.l), go, device)
-    cfK, cfV = _context_free(wl, K0, V0, device)
+    cfK, cfV = _context_free(wl, K0, V0, device) if context_free else (None, None)
     omega_c = None
     if wl.summary_mode == "rank":
         omega_c = _randn((d, wl.l_c), _generator(device, wl, "omega_c"), device)
     return WorkloadInputs(wl=wl, exact_K=exact_K, exact_V=exact_V, edges=edge_inputs,
                           omega=omega, planted_ratio=(_seg_ratio(wl, False), _seg_ratio(wl, True)),
                           context_free_K=cfK, context_free_V=cfV, omega_c=omega_c)
+
+
+def _summaries(wl: Workload, kmean: torch.Tensor, g: torch.Generator, device) -> torch.Tensor:
+    """[L, H, A, d] anchor summaries of one segment: the key mean of the
+    preceding agent's exact cache plus a perturbation of N(0, s^2) scale per
+    component (s = summary_noise), drawn so that the anchors' similarity
+    order is planted with a margin.
+
+    The perturbation of anchor a is c_a * m_hat + p_a, with m_hat the unit
+    key mean.  Its component along the mean is c_a = z_a + rank(z_a) * gap,
+    z_a ~ N(0, s^2): the ranks of the z_a are kept and consecutive c are at
+    least gap = 0.4 s apart.  Its orthogonal part p_a has a uniformly random
+    direction orthogonal to m_hat and the expected norm of an N(0, s^2 I)
+    vector in d - 1 dimensions, s sqrt(d - 1).  Every summary then has the
+    same distance s sqrt(d - 1) from the line through the mean, so any
+    increasing function of the projection ordering anchors by closeness to the
+    mean direction orders them by c_a, with gaps fixed by the draw rather
+    than left to chance (the decision margins of exact anchor selection)."""
+    L, H, d = kmean.shape
+    A = wl.A
+    sdev = wl.summary_noise
+    norm = torch.linalg.vector_norm(kmean, dim=-1, keepdim=True)
+    mhat = torch.where(norm > 0, kmean / norm.clamp_min(1e-30), torch.zeros_like(kmean))
+    z = sdev * _randn((L, H, A), g, device)
+    rank = torch.argsort(torch.argsort(z, dim=-1), dim=-1).to(torch.float32)
+    c = z + rank * (0.4 * sdev)
+    e = _randn((L, H, A, d), g, device)
+    e = e - (e * mhat.unsqueeze(2)).sum(-1, keepdim=True) * mhat.unsqueeze(2)
+    en = torch.linalg.vector_norm(e, dim=-1, keepdim=True).clamp_min(1e-30)
+    p = e * (sdev * math.sqrt(max(d - 1, 1)) / en)
+    return kmean.unsqueeze(2) + c.unsqueeze(-1) * mhat.unsqueeze(2) + p
 
 
 def _spectral_keys(wl: Workload, T: int, g: torch.Generator, device) -> torch.Tensor:

@@ -344,24 +344,30 @@ kvc_status kvc_chain_edge(int32_t edge, const kvc_segments* seg, const kvc_param
  * whose memory manager owns all of the GPU's memory and exposes no
  * allocation hook, or a serving loop that forbids allocation on the request
  * path because cudaMalloc/cudaFree can synchronise the device.  This variant
- * takes the per-unit norm scratch from a 4 MiB device array inside the
- * library (created when the library's device code is loaded, held until
- * process exit) instead of a caller workspace; every input and output is
- * still the caller's.  It allocates nothing and otherwise behaves exactly
- * like kvc_chain_edge (same arguments minus the workspace, same results).
+ * takes its scratch (the per-unit norms; in summary_mode 1 also the query
+ * representations) from a 4 MiB device array inside the library instead of a
+ * caller workspace; every input and output is still the caller's.  It
+ * allocates nothing and otherwise behaves exactly like kvc_chain_edge (same
+ * arguments minus the workspace, bit-identical results).
  *
  * Limits and rules:
- *   - S * L * H must not exceed KVC_NOALLOC_MAX_UNITS, else the call returns
- *     KVC_ERR_WORKSPACE with a message, before anything is launched; in
- *     summary_mode 1 the query representations must fit as well (d * r_C
- *     more floats per unit), else KVC_ERR_WORKSPACE;
- *   - the first call on a device (any edge) looks up the array's device
- *     address for that device; make that first call before any stream
- *     capture;
- *   - all calls on a device share the array: calls whose work may overlap on
- *     the GPU (unordered streams) race on it and must be serialised by the
- *     caller.  Each call writes every scratch entry it reads, so nothing needs
- *     clearing between calls.
+ *   - the scratch kvc_chain_edge_workspace() would ask for must fit in the
+ *     4 MiB array: S * L * H <= KVC_NOALLOC_MAX_UNITS in summary_mode 0,
+ *     and about 4 MiB / (16 + 4 * d * r_C) bytes' worth of units in
+ *     summary_mode 1 (255 units at d = 128, r_C = 32).  A larger call returns
+ *     KVC_ERR_WORKSPACE, naming the static scratch limit, before anything is
+ *     launched;
+ *   - the array belongs to the CUDA context current on the calling thread:
+ *     each context that loads the library holds its own copy until the
+ *     context is destroyed (process exit for a device's primary context).
+ *     The first call in a context (any edge) looks up the array's device
+ *     address in that context; make that first call before any stream
+ *     capture.  Later calls in the same context reuse the address; a new
+ *     context (for example after cudaDeviceReset) gets a fresh lookup;
+ *   - all calls in one context share the array: calls whose work may overlap
+ *     on the GPU (unordered streams) race on it and must be serialised by the
+ *     caller.  Each call writes every scratch entry it reads, so nothing
+ *     needs clearing between calls.
  * ------------------------------------------------------------------------- */
 #define KVC_NOALLOC_MAX_UNITS 262144
 kvc_status kvc_chain_edge_noalloc(int32_t edge, const kvc_segments* seg, const kvc_params* prm,

@@ -61,6 +61,59 @@ def sim_gaps(query: np.ndarray, summaries: np.ndarray) -> np.ndarray:
     return gaps
 
 
+def sim_table(query: np.ndarray, summaries: np.ndarray) -> np.ndarray:
+    """[S, L, H, A] oracle similarities of every anchor (cosine of mean keys,
+    or the Gram cosine of representations for [S, L, H, A, d, r_C])."""
+    S, L, H, A = summaries.shape[:4]
+    sim = O.rep_similarity if summaries.ndim == 6 else O.cosine
+    out = np.empty((S, L, H, A))
+    for s in range(S):
+        for l in range(L):
+            for h in range(H):
+                for a in range(A):
+                    out[s, l, h, a] = sim(query[s, l, h], summaries[s, l, h, a])
+    return out
+
+
+def check_decisions(best_gpu: np.ndarray, weights_gpu: np.ndarray, orc: Dict, summaries,
+                    top_k: int, gap_min: float, expect_decided: bool = True) -> int:
+    """Best anchor and kept (top-k) anchor set of EVERY unit.
+
+    A unit is decided when the oracle's similarity gap at the argmax (top-2)
+    and at the top-k boundary is >= gap_min: there the GPU's best anchor and
+    its set of anchors with nonzero weight must equal the oracle's exactly.
+    In an undecided unit several answers are correct: the GPU's best must be
+    an anchor within gap_min of the maximum similarity, and every anchor it
+    keeps must be within gap_min of the k-th largest similarity or above it.
+    Returns the number of undecided units; with ``expect_decided`` (the
+    generator plants similarity margins for mean-key summaries) it must be 0."""
+    sims = sim_table(orc["query"], summaries)
+    S, L, H, A = sims.shape
+    k = min(top_k, A)
+    undecided = 0
+    for s in range(S):
+        for l in range(L):
+            for h in range(H):
+                v = sims[s, l, h]
+                order = sorted(range(A), key=lambda a: (-v[a], a))
+                top2 = v[order[0]] - v[order[1]] if A > 1 else np.inf
+                kgap = v[order[k - 1]] - v[order[k]] if k < A else np.inf
+                kept_g = weights_gpu[s, l, h] > 0
+                kept_o = orc["weights"][s, l, h] > 0
+                if top2 >= gap_min and kgap >= gap_min:
+                    assert int(best_gpu[s, l, h]) == int(orc["best"][s, l, h]), (s, l, h, v)
+                    assert np.array_equal(kept_g, kept_o), (s, l, h, v)
+                    continue
+                undecided += 1
+                b = int(best_gpu[s, l, h])
+                assert v[b] >= v[order[0]] - gap_min, (s, l, h, b, v)
+                assert int(kept_g.sum()) == k, (s, l, h, kept_g)
+                assert np.all(v[kept_g] >= v[order[k - 1]] - gap_min), (s, l, h, v)
+    if expect_decided:
+        assert undecided == 0, "%d undecided units" % undecided
+    return undecided
+
+
 def unit_errors(wl: synth.Workload, out_gpu: np.ndarray, out_orc: np.ndarray, ref_orc: np.ndarray):
     """Per (segment, layer, head): (|gpu - oracle|_F, |C_oracle|_F, |oracle|_F) on PH rows."""
     rows = []

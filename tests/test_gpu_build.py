@@ -182,10 +182,28 @@ def test_chain_with_builder_matches_oracle(name):
                         err = np.linalg.norm(g - o)
                         bound = (2e-2 if bf16 else 1e-4) * c + (j * 2.0 ** -8 if bf16 else 1e-6) * np.linalg.norm(o)
                         assert err <= bound, (j, s, layer, h, err, c)
+        # effective ranks: exact wherever the oracle's cumulative energy
+        # fraction is >= 1e-3 from energy_frac at the deciding index
         er_g = eo.eff_rank.cpu().numpy()
         er_o = res[j]["eff_rank"]
-        agree = float(np.mean(er_g == er_o))
-        assert agree >= 0.9, (j, er_g, er_o)
+        sv_o = res[j]["sigma"]
+        masked = 0
+        for s in range(wl.S):
+            q, t0, n = wl.seg_request[s], wl.seg_start[s], wl.seg_len[s]
+            for layer in range(wl.L):
+                for h in range(wl.H):
+                    for kv, key in ((0, "out_K"), (1, "out_V")):
+                        E = (inp.exact_K if kv == 0 else inp.exact_V)[j]
+                        delta = np64(E[q, layer, h, t0:t0 + n]) - res[j - 1][key][q, layer, h, t0:t0 + n]
+                        total = float(np.sum(delta * delta))
+                        ero = int(er_o[s, layer, h, kv])
+                        if _margin_ok(sv_o[s, layer, h, kv], total, wl.energy_frac, ero):
+                            assert int(er_g[s, layer, h, kv]) == ero, (j, s, layer, h, kv)
+                        else:
+                            masked += 1
+        print("edge %d: effective ranks compared on %d of %d states" %
+              (j, er_o.size - masked, er_o.size))
+        assert masked <= er_o.size // 10, (j, masked)
 
 
 @pytest.mark.parametrize("name", ["tiny-f32", "longctx-small"])

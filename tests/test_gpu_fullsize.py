@@ -16,7 +16,7 @@ import torch
 from agent_shared_context_gb300 import synth
 from agent_shared_context_gb300.synth import EdgeInputs, WorkloadInputs
 
-from ._harness import check_out, np64, oracle_chain, sim_gaps
+from ._harness import check_decisions, check_out, np64, oracle_chain
 
 pytestmark = pytest.mark.gpu
 
@@ -49,6 +49,55 @@ def restrict(wl, inp, q, segs):
                                omega_c=inp.omega_c)
 
 
+def restrict_rows(wl, inp, segs):
+    """Sub-workload of the listed segments (any requests), their rows packed
+    back to back into one request: the oracle then holds only those rows."""
+    lens = [wl.seg_len[s] for s in segs]
+    starts = [sum(lens[:i]) for i in range(len(segs))]
+    sub = dataclasses.replace(
+        wl, R=1, T=sum(lens), name=wl.name + "-rows",
+        seg_request=tuple(0 for _ in segs), seg_start=tuple(starts), seg_len=tuple(lens))
+
+    def rows(E):
+        return torch.cat([E[wl.seg_request[s]:wl.seg_request[s] + 1, :, :,
+                            wl.seg_start[s]:wl.seg_start[s] + wl.seg_len[s]] for s in segs], dim=3)
+
+    idx = torch.tensor(segs, device=inp.exact_K[0].device)
+    Tm = sub.max_seg_len
+    edges = [None if e is None else EdgeInputs(
+        U_K=e.U_K.index_select(0, idx)[:, :, :, :Tm].contiguous(),
+        W_K=e.W_K.index_select(0, idx),
+        U_V=e.U_V.index_select(0, idx)[:, :, :, :Tm].contiguous(),
+        W_V=e.W_V.index_select(0, idx),
+        summaries=e.summaries.index_select(0, idx),
+        planted=e.planted[segs],
+        reps=None if e.reps is None else e.reps.index_select(0, idx)) for e in inp.edges]
+    return sub, rows, WorkloadInputs(wl=sub, exact_K=[rows(E) for E in inp.exact_K],
+                                     exact_V=[rows(E) for E in inp.exact_V], edges=edges,
+                                     omega=inp.omega, planted_ratio=inp.planted_ratio,
+                                     omega_c=inp.omega_c)
+
+
+def _compare_edge(j, eo, sub, rows, res, summ, segs):
+    """Edge j of the full-size run against the oracle chain of the sampled
+    segments: flags, scores, weights, every unit's decisions, outputs."""
+    fb_g = eo.fallback.cpu().numpy().astype(bool)[segs]
+    assert np.array_equal(fb_g, res[j]["fallback"]), (j, fb_g, res[j]["score"])
+    np.testing.assert_allclose(eo.score.cpu().numpy()[segs], res[j]["score"],
+                               rtol=2e-3 if j == 1 else 1e-2)
+    w_g = eo.weights.cpu().numpy()[segs]
+    if j == 1:
+        np.testing.assert_allclose(w_g, res[j]["weights"], rtol=0, atol=2e-4)
+    else:
+        np.testing.assert_allclose(w_g, res[j]["weights"], rtol=1e-2, atol=1e-4)
+    undecided = check_decisions(eo.best.cpu().numpy()[segs], w_g, res[j], summ[j - 1], sub.k_top,
+                                1e-5 if j == 1 else 1e-3)
+    for key in ("out_K", "out_V"):
+        out_g = np64(rows(getattr(eo, key)))
+        check_out(sub, j, out_g, res[j][key], res[j - 1][key], res[j]["fallback"], True)
+    return undecided
+
+
 def _compare(wl, runner, sub, sub_inp, q, segs, build):
     res, (_, _, _, _, summ) = oracle_chain(sub, sub_inp, build=build)
     for j in range(1, wl.edges + 1):
@@ -64,9 +113,10 @@ def _compare(wl, runner, sub, sub_inp, q, segs, build):
         else:
             np.testing.assert_allclose(w_g, res[j]["weights"], rtol=1e-2 if not build else 5e-2,
                                        atol=1e-4 if not build else 1e-3)
-            gap = 2e-3
-        sure = sim_gaps(res[j]["query"], summ[j - 1]) >= gap
-        assert np.array_equal(eo.best.cpu().numpy()[segs][sure], res[j]["best"][sure])
+            gap = 1e-3
+        undecided = check_decisions(eo.best.cpu().numpy()[segs], w_g, res[j], summ[j - 1],
+                                    sub.k_top, gap, expect_decided=sub.summary_mode == "mean")
+        print("edge %d: undecided units %d of %d" % (j, undecided, sub.S * sub.L * sub.H))
         for key in ("out_K", "out_V"):
             out_g = np64(getattr(eo, key)[q:q + 1])
             if not build:
@@ -113,21 +163,43 @@ def test_llama2k_full_size_sampled_requests():
         _compare(wl, runner, sub, sub_inp, q, segs, build=False)
 
 
-def test_concurrent_full_size_first_edge_sampled_segments():
-    wl = dataclasses.replace(synth.workload("concurrent"), n_agents=2)
-    inp, runner = _run(wl)
-    q = 0
-    segs = [s for s in range(wl.S) if wl.seg_request[s] == q][:3]
-    sub, sub_inp = restrict(wl, inp, q, segs)
-    _compare(wl, runner, sub, sub_inp, q, segs, build=False)
-    # PF rows of every request are untouched by the whole-batch call
-    eo = runner.edges[1]
-    mask = torch.ones((wl.R, wl.T), dtype=torch.bool)
+def test_concurrent_full_size_chain_sampled_segments():
+    """The concurrent serving batch at full size (16 requests x 16 segments of
+    512 PH tokens behind 128-token PF segments, 32 x 8 x 128 bf16, 8 anchors)
+    through all three edges A0 -> A1 -> A2 -> A3, with the two alternating
+    output buffers the bench uses.  Sampled segments of three requests --
+    among them a planted fallback segment of every edge -- are recomputed by
+    the oracle's chain; PF rows are never written."""
+    from agent_shared_context_gb300.chain import ChainRunner
+    wl = synth.workload("concurrent")
+    inp = synth.generate(wl, device="cuda", context_free=False)
+    runner = ChainRunner(wl, inp, device="cuda", keep_outputs=False)
+    segs = {0, 1, 17, wl.S - 1}                       # requests 0, 1 and 15
+    for e in inp.edges:
+        segs.add(int(torch.nonzero(e.planted)[0]))    # a planted fallback of every edge
+    segs = sorted(segs)
+    assert len({wl.seg_request[s] for s in segs}) >= 2
+    sub, rows, sub_inp = restrict_rows(wl, inp, segs)
+    res, (_, _, _, _, summ) = oracle_chain(sub, sub_inp)
+    pf = torch.ones((wl.R, wl.T), dtype=torch.bool)
     for s in range(wl.S):
-        mask[wl.seg_request[s], wl.seg_start[s]:wl.seg_start[s] + wl.seg_len[s]] = False
-    for r in range(wl.R):
-        pf = mask[r].cuda()
-        assert torch.equal(eo.out_K[r][:, :, pf, :], inp.exact_K[1][r][:, :, pf, :])
+        pf[wl.seg_request[s], wl.seg_start[s]:wl.seg_start[s] + wl.seg_len[s]] = False
+    pf = pf.cuda()
+    flagged = 0
+    for j in range(1, wl.edges + 1):
+        runner.run_edge(j)
+        torch.cuda.synchronize()
+        assert int(runner.dev_status.item()) == 0
+        eo = runner.edges[j]
+        assert int(eo.fallback.sum()) == int(round(wl.fallback_frac * wl.S))
+        flagged += int(res[j]["fallback"].sum())
+        undecided = _compare_edge(j, eo, sub, rows, res, summ, segs)
+        print("edge %d: %d sampled segments, undecided units %d" % (j, len(segs), undecided))
+        # PF rows keep the prefix of the agent the buffer was created for
+        owner = 1 if j % 2 == 1 else 2
+        for r in (0, wl.R - 1):
+            assert torch.equal(eo.out_K[r][:, :, pf[r], :], inp.exact_K[owner][r][:, :, pf[r], :])
+    assert flagged >= wl.edges
 
 
 def test_vl_full_size_sampled_segments_with_tail():

@@ -79,8 +79,9 @@ def test_carrying_ksum_decides_like_rereading_the_keys(name):
         assert torch.equal(ea.fallback, eb.fallback), j
         np.testing.assert_allclose(ea.weights.cpu().numpy(), eb.weights.cpu().numpy(),
                                    rtol=0, atol=1e-5)
-        same_best = float((ea.best == eb.best).float().mean())
-        assert same_best >= 0.999, (j, same_best)
+        # the generator plants similarity margins far above the fp32 summation
+        # difference, so every best anchor agrees
+        assert torch.equal(ea.best, eb.best), j
         for key in ("out_K", "out_V"):
             x = getattr(ea, key).double()
             y = getattr(eb, key).double()

@@ -2,11 +2,15 @@
 
 Every case generates one seeded workload on the GPU, runs the library through
 the C ABI, and runs the oracle on the same input tensors (copied to the host
-and upcast exactly to float64).  Decisions (best anchor, fallback flags) must
-match exactly -- the generator keeps segment scores >= 25% away from tau, and
-best-anchor comparisons skip only units whose oracle top-2 similarity gap is
-below 1e-5 (there either anchor is a valid argmax); floats follow the
-tolerances documented in ``tests/_harness.check_out``.
+and upcast exactly to float64).  Decisions must match exactly: fallback flags
+(the generator keeps segment scores >= 25% away from tau), and the best
+anchor and kept top-k set of every unit (the generator plants a similarity
+margin between the anchors' summaries; ``_harness.check_decisions`` checks
+every unit and requires 0 undecided ones except in the cases listed in
+``UNDECIDED_OK``, where segments of <= 24 tokens make the key mean large
+against the N(0, 0.1^2) summary perturbation, so the planted margins shrink
+below the threshold and any near-maximal anchor is a valid answer); floats
+follow the tolerances documented in ``tests/_harness.check_out``.
 """
 import math
 
@@ -17,7 +21,7 @@ import torch
 import oracle as O
 from agent_shared_context_gb300 import synth
 
-from ._harness import check_out, np64, oracle_chain, oracle_inputs, sim_gaps
+from ._harness import check_decisions, check_out, np64, oracle_chain, oracle_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -74,6 +78,8 @@ def dataclass_replace(wl, **kw):
 
 
 CASES = list(_cases().keys())
+# cases with segments of <= 24 tokens (see the module docstring)
+UNDECIDED_OK = {"short-segments", "max-segments"}
 
 
 @pytest.mark.parametrize("name", CASES)
@@ -82,13 +88,15 @@ def test_chain_matches_oracle(name):
 
     Edge 1 sees the same reference on both sides (the exact A0 cache), so
     weights must agree to 2e-4 (bf16) / 2e-5 (f32) and best anchors exactly
-    wherever the oracle's top-2 similarity gap is >= 1e-5.  From edge 2 on,
-    the GPU's reference is its own bf16 output of the previous edge while the
+    wherever the oracle's similarity gaps are >= 1e-5.  From edge 2 on, the
+    GPU's reference is its own bf16 output of the previous edge while the
     oracle's is unrounded fp64: bf16 RNE perturbs each held element by up to
-    2^-9 relative, which moves the mean-pooled query by ~2^-9 / sqrt(3)
-    relative and the softmax weights by ~that / temperature; weights then get
-    rtol 1e-2 + atol 1e-4 and best anchors are compared where the gap is
-    >= 2e-3.  Outputs follow check_out (its bound grows with the edge)."""
+    2^-9 relative, which moves the mean-pooled query by ~2^-9 / sqrt(3 n)
+    per component and a cosine by ~1e-4, and the softmax weights by ~that /
+    temperature; weights then get rtol 1e-2 + atol 1e-4 and decisions need a
+    gap of 1e-3 (the survey's decision margin).  Every unit is checked
+    (``check_decisions``).  Outputs follow check_out (its bound grows with
+    the edge)."""
     kvc = _kvc()
     from agent_shared_context_gb300.chain import ChainRunner
     wl = _cases()[name]
@@ -119,10 +127,10 @@ def test_chain_matches_oracle(name):
             gap_min = 1e-5
         else:
             np.testing.assert_allclose(w_gpu, orc["weights"], rtol=1e-2, atol=1e-4)
-            gap_min = 2e-3
-        best = eo.best.cpu().numpy()
-        sure = sim_gaps(orc["query"], summ[j - 1]) >= gap_min
-        assert np.array_equal(best[sure], orc["best"][sure]), report
+            gap_min = 1e-3
+        undecided = check_decisions(eo.best.cpu().numpy(), w_gpu, orc, summ[j - 1], wl.k_top,
+                                    gap_min, expect_decided=name not in UNDECIDED_OK)
+        print("edge %d: undecided units %d of %d" % (j, undecided, wl.S * wl.L * wl.H))
         refK = res[j - 1]["out_K"]
         refV = res[j - 1]["out_V"]
         check_out(wl, j, np64(eo.out_K), orc["out_K"], refK, fb_orc, bf16)
@@ -169,8 +177,8 @@ def test_match_alone(name):
                                  np64(e.summaries), wl.k_top, wl.temperature)
     np.testing.assert_allclose(qv.cpu().numpy(), oq, rtol=0, atol=1e-5)
     np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=0, atol=2e-5)
-    sure = sim_gaps(oq, np64(e.summaries)) >= 1e-5
-    assert np.array_equal(b.cpu().numpy()[sure], ob[sure])
+    check_decisions(b.cpu().numpy(), w.cpu().numpy(), dict(query=oq, weights=ow, best=ob),
+                    np64(e.summaries), wl.k_top, 1e-5)
     # determinism: a second run is bit-identical
     w2 = torch.empty_like(w)
     b2 = torch.empty_like(b)
@@ -237,6 +245,82 @@ def test_apply_one_hot_and_random_weights(name):
         check_out(wl, 1, np64(oV), cV, EV[0], np.zeros(wl.S, bool), bf16)
         np.testing.assert_allclose(part.cpu().numpy(), opart, rtol=3e-2 if bf16 else 1e-5, atol=1e-6)
         np.testing.assert_allclose(score.cpu().numpy(), osc, rtol=1e-2 if bf16 else 1e-5)
+
+
+def _bf16_rne(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bf16 (ties to even), as float64.
+    Round-to-odd to float32 first (so the second rounding cannot double-round),
+    then RNE on the 16 dropped bits."""
+    f = x.astype(np.float32)
+    lo = np.nextafter(f, np.float32(-np.inf))
+    hi = np.nextafter(f, np.float32(np.inf))
+    # round to odd: an inexact float32 result keeps the neighbour with an odd mantissa
+    inexact = f.astype(np.float64) != x
+    below = f.astype(np.float64) > x
+    cand = np.where(below, lo, f)
+    cand2 = np.where(below, f, hi)
+    odd = (cand.view(np.uint32) & 1) == 1
+    f = np.where(inexact, np.where(odd, cand, cand2), f)
+    b = f.view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("A,r,weights", [(1, 32, "pow2"), (8, 32, "pow2"), (8, 32, "softmax"),
+                                         (32, 16, "pow2"), (32, 16, "softmax")])
+def test_apply_zero_reference_elementwise(A, r, weights):
+    """ref = 0 makes out = RNE_bf16(C): every element of a 512-row segment
+    (four full 128-token tiles) against the oracle's exact C.
+
+    With power-of-two weights the fold w * W is exact in bf16, the products
+    of bf16 operands are exact in fp32, and the tensor core only accumulates:
+    |out - C| <= 2^-8 |C| (one RNE) + 2^-14 S per element, S = sum_k |U_tk|
+    |w W_nk| (an fp32 accumulation allowance for K <= 512 terms), and out must
+    equal the correctly rounded RNE_bf16(C) except where the accumulation lands
+    across a rounding boundary (at most 1 in 1,000 elements).  With general
+    (softmax) weights the fold rounds w * W once more: the allowance grows by
+    2^-8 S."""
+    kvc = _kvc()
+    wl = synth.scaled(synth.workload("llama2k"), L=1, H=2, R=1, seg_len=[512], A=A, r=r,
+                      top_k=A, fallback_frac=0.0)
+    inp = _edge1_setup(wl)
+    seg, EK, EV, states, summ = oracle_inputs(wl, inp)
+    if weights == "pow2":
+        wv = [2.0 ** -(a + 1) for a in range(A)]
+        wv[-1] = wv[-2] if A > 1 else 1.0                 # sums to 1, all powers of two
+        w = torch.tensor(wv, device="cuda").expand(wl.S, wl.L, wl.H, A).contiguous()
+    else:
+        g = torch.Generator(device="cuda")
+        g.manual_seed(11)
+        w = torch.softmax(torch.randn((wl.S, wl.L, wl.H, A), generator=g, device="cuda") / 0.3, -1)
+    zK = torch.zeros_like(inp.exact_K[0])
+    zV = torch.zeros_like(inp.exact_V[0])
+    oK, oV, part, score, fb = _apply(kvc, wl, inp, w, ref=(zK, zV))
+    wk = np64(w)
+    zero = np.zeros_like(EK[0])
+    cK, cV, _ = O.apply_correction((zero, zero), seg, states[0], wk)
+    f = 2.0 ** -14 if weights == "pow2" else 2.0 ** -8 + 2.0 ** -14
+    n = wl.seg_len[0]
+    mismatches = total = 0
+    for kv, (out, C) in enumerate(((oK, cK), (oV, cV))):
+        Ug = states[0].U[kv]
+        Wg = states[0].W[kv]
+        for h in range(wl.H):
+            g_out = np64(out[0, 0, h, :n])
+            c = C[0, 0, h, :n]
+            S = np.zeros_like(c)
+            for a in range(A):
+                S += np.abs(Ug[0, 0, h, :n, a, :]) @ (np.abs(wk[0, 0, h, a]) *
+                                                      np.abs(Wg[0, 0, h, :, a, :])).T
+            bound = 2.0 ** -8 * np.abs(c) + (1 + 2.0 ** -8) * f * S
+            err = np.abs(g_out - c)
+            assert np.all(err <= bound), (kv, h, float((err - bound).max()))
+            exact = _bf16_rne(c)
+            mismatches += int(np.sum(g_out != exact))
+            total += c.size
+    print("A=%d %s: %d of %d elements differ from RNE_bf16(C)" % (A, weights, mismatches, total))
+    if weights == "pow2":
+        assert mismatches <= total // 1000, mismatches
 
 
 def test_apply_deterministic():

@@ -22,7 +22,7 @@ import torch
 import oracle as O
 from agent_shared_context_gb300 import synth
 
-from ._harness import check_out, np64
+from ._harness import check_decisions, check_out, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -110,16 +110,19 @@ def test_match_representation_matches_oracle_on_shared_inputs():
     kvc.kvc_match_representation(seg, prm, qrep, anchors, w, b, st)
     torch.cuda.synchronize()
     qn, an = np64(qrep), np64(anchors)
+    wo_all = np.zeros((S, L, H, A))
+    bo_all = np.zeros((S, L, H), dtype=np.int64)
     for s in range(S):
         for layer in range(L):
             for h in range(H):
                 sims = [O.rep_similarity(qn[s, layer, h], an[s, layer, h, a]) for a in range(A)]
                 wo, bo = O.select_and_weight(sims, wl.k_top, wl.temperature)
                 np.testing.assert_allclose(w[s, layer, h].cpu().numpy(), wo, rtol=0, atol=2e-5)
-                srt = sorted(sims, reverse=True)
-                if srt[0] - srt[1] >= 1e-5:
-                    assert int(b[s, layer, h]) == bo
-                assert int((w[s, layer, h] > 0).sum()) == wl.k_top
+                wo_all[s, layer, h] = wo
+                bo_all[s, layer, h] = bo
+    # every unit's best anchor and kept set (exact where the gaps are >= 1e-5)
+    check_decisions(b.cpu().numpy(), w.cpu().numpy(), dict(query=qn, weights=wo_all, best=bo_all),
+                    an, wl.k_top, 1e-5, expect_decided=False)
 
 
 @pytest.mark.parametrize("name", ["bf16-d128-rc32", "f32-d64-rc16"])
@@ -145,15 +148,12 @@ def test_chain_in_representation_mode_matches_oracle(name):
         assert np.array_equal(fb, res[j]["fallback"]), (j, fb, res[j]["score"])
         np.testing.assert_allclose(eo.score.cpu().numpy(), res[j]["score"], rtol=1e-2)
         np.testing.assert_allclose(eo.weights.cpu().numpy(), res[j]["weights"], rtol=0, atol=5e-4)
-        # best anchors where the oracle's top-2 similarity gap is clear
-        qr = res[j]["query"]
-        for s in range(wl.S):
-            for layer in range(wl.L):
-                for h in range(wl.H):
-                    sims = sorted((O.rep_similarity(qr[s, layer, h], reps[j - 1][s, layer, h, a])
-                                   for a in range(wl.A)), reverse=True)
-                    if sims[0] - sims[1] >= 2e-3:
-                        assert int(eo.best[s, layer, h]) == int(res[j]["best"][s, layer, h])
+        # every unit: exact where the oracle's similarity gaps are >= 2e-3,
+        # else a near-maximal anchor (representation similarities carry no
+        # planted margin, so undecided units are counted, not forbidden)
+        undecided = check_decisions(eo.best.cpu().numpy(), eo.weights.cpu().numpy(), res[j],
+                                    reps[j - 1], wl.k_top, 2e-3, expect_decided=False)
+        print("edge %d: undecided units %d of %d" % (j, undecided, wl.S * wl.L * wl.H))
         for key in ("out_K", "out_V"):
             check_out(wl, j, np64(getattr(eo, key)), res[j][key], res[j - 1][key],
                       res[j]["fallback"], bf16)
