@@ -6,19 +6,25 @@
 // is the skinny product C[n, d] = U[n, A*r] . (w (.) W)[A*r, d]^T, where the
 // anchor weights are folded into W once per item.  Per 128-token tile:
 //
-//   warp 0 (1 thread)  TMA: the item's W chunks (once) and the U chunks (64
-//                      columns = one 128-byte swizzle row each) into a
-//                      shared-memory ring guarded by mbarriers;
+//   warp 0 (1 thread)  TMA: the U chunks (64 columns = one 128-byte swizzle
+//                      row each) into a shared-memory ring;
+//   warps 8-11         the W pipeline: one thread issues the TMA loads of the
+//                      items' W chunks into a ring of chunk slots (as soon as
+//                      a slot is free, running ahead into the next items), all
+//                      128 threads fold the anchor weights into each landed
+//                      chunk in place (bf16, RNE) and mark it ready, so the
+//                      next item's W is loaded and folded while the current
+//                      item's tiles stream;
 //   warp 6 (1 thread)  TMA: the ref tiles into their own ring, so U
 //                      prefetch never waits for a ref buffer;
 //   warp 1 (1 thread)  tcgen05.mma kind::f16, M = 128 tokens, N = d,
 //                      K = A*r in steps of 16, accumulating in TMEM (two
 //                      accumulator buffers so tile t+1's MMAs overlap tile
-//                      t's epilogue);
+//                      t's epilogue); after an item's last tile it releases
+//                      each W chunk slot as its MMAs complete;
 //   warp 7             the K output tiles' column sums (below);
-//   warps 2-5          fold the weights into W in place (bf16, RNE) once per
-//                      item; per tile read the fp32 accumulator rows from
-//                      TMEM (thread = token row), add the ref row from shared
+//   warps 2-5          per tile read the fp32 accumulator rows from TMEM
+//                      (thread = token row), add the ref row from shared
 //                      memory, round to bf16 (RNE), accumulate |C|^2 and
 //                      |ref|^2, write the result over the ref tile and TMA-
 //                      store it (full tiles) or store the valid rows with
@@ -42,6 +48,8 @@
 // and returns.
 #include <cuda_bf16.h>
 
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "kvc_internal.h"
@@ -55,10 +63,13 @@ using namespace ptx;
 constexpr int kBM = 128;                   // tokens per tile (MMA M)
 constexpr int kChunk = 64;                 // bf16 per 128-byte swizzled row
 constexpr int kUStageBytes = kBM * 128;    // one U chunk: 128 rows x 128 B
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;              // 12 warps (roles above)
 constexpr int kMaxUStages = 8;
 constexpr int kMaxRefBufs = 3;
+constexpr int kMaxWSlots = 16;
 constexpr int kEpiThreads = 128;
+constexpr int kWgThreads = 128;
+constexpr int kWgFirst = 256;              // first thread of the W pipeline (warp 8)
 
 struct TcMaps {
   CUtensorMap ref[2];
@@ -74,18 +85,22 @@ struct TcArgs {
   float* partial;            // [units, 4]
   float* ksum;               // [units, 4, D] column sums of the K output rows, or nullptr
   int32_t* dev_status;
-  int32_t L, H, A, r, K, KC, n_items, n_ustages, n_refbufs;
+  int32_t L, H, A, r, K, KC, n_items, n_ustages, n_refbufs, n_wslots;
 };
 
 struct Bars {
-  uint64_t w_full, w_ready, w_free, mma_drain;
+  uint64_t mma_drain;
   uint64_t acc_full[2], acc_empty[2];
   uint64_t u_full[kMaxUStages], u_empty[kMaxUStages];
   uint64_t ref_full[kMaxRefBufs], ref_empty[kMaxRefBufs];
   uint64_t tile_done[kMaxRefBufs];   // the epilogue has written the output tile in place
+  uint64_t w_full[kMaxWSlots];       // a W chunk landed in its slot
+  uint64_t w_ready[kMaxWSlots];      // ... and carries the folded weights
+  uint64_t w_free[kMaxWSlots];       // the MMAs of the slot's last tile completed
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t epi_ok[2];
+  int32_t wg_ok[2];
   float red[2][4];
 };
 
@@ -152,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* w_smem = smem;
-  uint8_t* u_smem = w_smem + a.KC * WCB;
+  uint8_t* u_smem = w_smem + a.n_wslots * WCB;
   uint8_t* r_smem = u_smem + a.n_ustages * kUStageBytes;
   Bars* bars = reinterpret_cast<Bars*>(r_smem + a.n_refbufs * REFB);
 
@@ -160,11 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int NSU = a.n_ustages;
   const int NRB = a.n_refbufs;
+  const int NWS = a.n_wslots;
+  const int KC = a.KC;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->w_full, 1);
-    mbar_init(&bars->w_ready, 1);
-    mbar_init(&bars->w_free, 1);
     mbar_init(&bars->mma_drain, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->acc_full[b], 1);
@@ -179,9 +193,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->ref_empty[i], 2);     // the store's release + the key-sum warp
       mbar_init(&bars->tile_done[i], 1);
     }
+    for (int i = 0; i < NWS; ++i) {
+      mbar_init(&bars->w_full[i], 1);
+      mbar_init(&bars->w_ready[i], 1);
+      mbar_init(&bars->w_free[i], 1);
+    }
     bars->abort_flag = 0;
     bars->epi_ok[0] = 1;
     bars->epi_ok[1] = 1;
+    bars->wg_ok[0] = 1;
+    bars->wg_ok[1] = 1;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -194,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ U producer
     if (lane == 0) {
       for (int kv = 0; kv < 2; ++kv) {
         tma_prefetch_desc(&maps.ref[kv]);
@@ -202,40 +223,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&maps.W[kv]);
         tma_prefetch_desc(&maps.out[kv]);
       }
-      uint32_t ust = 0, uph = 0, wfree_ph = 0;
+      uint32_t ust = 0, uph = 0;
       uint32_t u_last[kMaxUStages];
       bool u_used[kMaxUStages];
       for (int i = 0; i < kMaxUStages; ++i) u_used[i] = false;
-      bool w_used = false;
-      uint32_t w_last = 0, w_issue_count = 0;
       bool ok = true;
-      const int w_after = a.KC < NSU ? a.KC : NSU;
       for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x) {
         const Item x = decode_item(it, a, seg);
-        bool w_issued = false;
-        int uc = 0;
-        auto issue_w = [&]() {
-          if (w_issue_count > 0) {
-            if (!wait_or_abort(&bars->w_free, wfree_ph, bars, a.dev_status)) {
-              ok = false;
-              return;
-            }
-            wfree_ph ^= 1u;
-          }
-          mbar_arrive_expect_tx(&bars->w_full, static_cast<uint32_t>(a.KC * WCB));
-          for (int kc = 0; kc < a.KC; ++kc)
-            tma_load_3d(w_smem + kc * WCB, &maps.W[x.kv], &bars->w_full, kc * kChunk, 0, x.unit);
-          w_last = w_issue_count & 1u;
-          w_used = true;
-          ++w_issue_count;
-          w_issued = true;
-        };
         for (int t = 0; t < x.ntiles && ok; ++t) {
-          for (int kc = 0; kc < a.KC; ++kc) {
-            if (!w_issued && uc == w_after) {
-              issue_w();
-              if (!ok) break;
-            }
+          for (int kc = 0; kc < KC; ++kc) {
             if (!wait_or_abort(&bars->u_empty[ust], uph ^ 1u, bars, a.dev_status)) {
               ok = false;
               break;
@@ -249,16 +245,88 @@ __global__ void __launch_bounds__(kThreads, 1)
               ust = 0;
               uph ^= 1u;
             }
-            ++uc;
           }
         }
-        if (ok && !w_issued) issue_w();
       }
       // Drain: every copy issued into this CTA's shared memory must land
       // before the CTA may exit (bounded; a no-op after normal completion).
       for (int i = 0; i < NSU; ++i)
         if (u_used[i]) (void)mbar_wait_bounded(&bars->u_full[i], u_last[i], kWaitLimitNs);
-      if (w_used) (void)mbar_wait_bounded(&bars->w_full, w_last, kWaitLimitNs);
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ W pipeline
+    // Chunk c of this CTA (c = local item k * KC + kc) lives in slot c mod NWS;
+    // its load waits until the MMAs of the chunk NWS earlier have completed.
+    const int wt = threadIdx.x - kWgFirst;    // 0..127
+    const int64_t my_items =
+        blockIdx.x < a.n_items ? (a.n_items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int64_t total = my_items * KC;
+    int64_t issued = 0;                       // thread 0's count of issued chunk loads
+    int64_t landed = 0;                       // chunks whose arrival thread 0 has seen
+    uint32_t n_waits = 0;
+    // issue the load of chunk c (thread 0 only); `block` waits for its slot
+    auto issue = [&](int64_t c, bool block) -> int {   // 1 issued, 0 not free, -1 abort
+      const int slot = static_cast<int>(c % NWS);
+      const uint32_t par = (static_cast<uint32_t>(c / NWS) & 1u) ^ 1u;
+      if (block) {
+        if (!wait_or_abort(&bars->w_free[slot], par, bars, a.dev_status)) return -1;
+      } else if (!mbar_test_wait(&bars->w_free[slot], par)) {
+        return 0;
+      }
+      const int it = blockIdx.x + static_cast<int>(c / KC) * gridDim.x;
+      const int kc = static_cast<int>(c % KC);
+      const Item x = decode_item(it, a, seg);
+      mbar_arrive_expect_tx(&bars->w_full[slot], static_cast<uint32_t>(WCB));
+      tma_load_3d(w_smem + slot * WCB, &maps.W[x.kv], &bars->w_full[slot], kc * kChunk, 0,
+                  x.unit);
+      return 1;
+    };
+    for (int64_t c = 0; c < total; ++c) {
+      const int slot = static_cast<int>(c % NWS);
+      const uint32_t par = static_cast<uint32_t>(c / NWS) & 1u;
+      volatile int32_t* flag = &bars->wg_ok[n_waits & 1u];
+      ++n_waits;
+      if (wt == 0) {
+        bool good = true;
+        while (good && issued <= c) {
+          good = issue(issued, true) == 1;
+          if (good) ++issued;
+        }
+        // run ahead into later chunks while their slots are free
+        while (good && issued < total && issued < c + NWS && issue(issued, false) == 1) ++issued;
+        if (good) good = wait_or_abort(&bars->w_full[slot], par, bars, a.dev_status);
+        if (good) landed = c + 1;
+        *flag = good ? 1 : 0;
+      }
+      named_sync(2, kWgThreads);
+      if (*flag == 0) break;
+      if (wt != 0) (void)mbar_wait_bounded(&bars->w_full[slot], par, kWaitLimitNs);
+      // fold the item's anchor weights into the chunk: 16-byte unit p of row
+      // n holds K-group p ^ (n & 7) (128-byte swizzle)
+      const int it = blockIdx.x + static_cast<int>(c / KC) * gridDim.x;
+      const int kc = static_cast<int>(c % KC);
+      const int unit = it >= (a.n_items >> 1) ? it - (a.n_items >> 1) : it;
+      const float* wts = a.weights + static_cast<int64_t>(unit) * a.A;
+      uint8_t* base = w_smem + slot * WCB;
+      for (int idx = wt; idx < WCB / 16; idx += kWgThreads) {
+        const int nrow = idx >> 3;
+        const int j = (idx & 7) ^ (nrow & 7);
+        const int k = kc * kChunk + j * 8;
+        if (k < a.K) {
+          uint4* p = reinterpret_cast<uint4*>(base + static_cast<size_t>(idx) * 16);
+          *p = scale_bf16x8(*p, __ldg(wts + k / a.r));
+        }
+      }
+      fence_proxy_async_smem();
+      named_sync(2, kWgThreads);
+      if (wt == 0) mbar_arrive(&bars->w_ready[slot]);
+    }
+    // Drain: loads issued ahead of the last seen arrival (fewer than NWS, one
+    // per slot) must land before the CTA exits.
+    if (wt == 0) {
+      for (int64_t c = landed; c < issued; ++c)
+        (void)mbar_wait_bounded(&bars->w_full[c % NWS], static_cast<uint32_t>(c / NWS) & 1u,
+                                kWaitLimitNs);
     }
   } else if (warp == 6) {
     // -------------------------------------------------------- ref producer
@@ -294,18 +362,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t ust = 0, uph = 0, wr_ph = 0, tile_count = 0;
+      uint32_t ust = 0, uph = 0, tile_count = 0;
       uint32_t acc_eph[2] = {0u, 0u};
       bool ok = true;
       bool issued_any = false;
-      for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x) {
+      int64_t c0 = 0;                          // first W chunk of the current item
+      for (int it = blockIdx.x; it < a.n_items && ok; it += gridDim.x, c0 += KC) {
         const Item x = decode_item(it, a, seg);
-        if (!wait_or_abort(&bars->w_ready, wr_ph, bars, a.dev_status)) {
-          ok = false;
-          break;
-        }
-        wr_ph ^= 1u;
-        tc_fence_after();
         for (int t = 0; t < x.ntiles && ok; ++t) {
           const uint32_t b = tile_count & 1u;
           if (!wait_or_abort(&bars->acc_empty[b], acc_eph[b] ^ 1u, bars, a.dev_status)) {
@@ -315,14 +378,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc_eph[b] ^= 1u;
           tc_fence_after();
           const uint32_t d_tmem = tmem + b * static_cast<uint32_t>(D);
-          for (int kc = 0; kc < a.KC; ++kc) {
+          for (int kc = 0; kc < KC; ++kc) {
+            const int64_t c = c0 + kc;
+            const int wslot = static_cast<int>(c % NWS);
+            if (t == 0) {
+              if (!wait_or_abort(&bars->w_ready[wslot], static_cast<uint32_t>(c / NWS) & 1u,
+                                 bars, a.dev_status)) {
+                ok = false;
+                break;
+              }
+            }
             if (!wait_or_abort(&bars->u_full[ust], uph, bars, a.dev_status)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t a_base = smem_u32(u_smem + ust * kUStageBytes);
-            const uint32_t b_base = smem_u32(w_smem + kc * WCB);
+            const uint32_t b_base = smem_u32(w_smem + wslot * WCB);
             const int rem = a.K - kc * kChunk;
             const int nks = rem >= kChunk ? 4 : (rem + 15) / 16;
             for (int ks = 0; ks < nks; ++ks) {
@@ -332,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             issued_any = true;
             mma_commit(&bars->u_empty[ust]);
+            if (t == x.ntiles - 1) mma_commit(&bars->w_free[wslot]);   // the slot's last use
             if (++ust == static_cast<uint32_t>(NSU)) {
               ust = 0;
               uph ^= 1u;
@@ -341,8 +414,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&bars->acc_full[b]);
           ++tile_count;
         }
-        if (!ok) break;
-        mma_commit(&bars->w_free);
       }
       // Drain: all MMAs issued by this thread complete before TMEM is freed.
       if (issued_any) {
@@ -416,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = threadIdx.x - 64;          // 0..127
     const int q = warp & 3;                   // TMEM lane quadrant of this warp
     const int m = q * 32 + lane;              // token row of the tile
-    uint32_t wf_ph = 0, rph = 0, rb = 0, tile_count = 0;
+    uint32_t rph = 0, rb = 0, tile_count = 0;
     uint32_t acc_fph[2] = {0u, 0u};
     uint32_t n_waits = 0;
     // One thread waits (bounded) and broadcasts the outcome through one of
@@ -440,30 +511,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int pending_rb = -1;
     for (int it = blockIdx.x; it < a.n_items; it += gridDim.x) {
       const Item x = decode_item(it, a, seg);
-      if (!epi_wait(&bars->w_full, wf_ph)) break;
-      wf_ph ^= 1u;
-      // Fold the anchor weights into W (in place, bf16 RNE).  W chunk kc
-      // holds D rows of 64 K-values; 16-byte unit p of row n holds K-group
-      // p ^ (n & 7) (128-byte swizzle).
-      {
-        const float* wts = a.weights + static_cast<int64_t>(x.unit) * a.A;
-        const int per_chunk = WCB / 16;
-        const int total = a.KC * per_chunk;
-        for (int idx = et; idx < total; idx += kEpiThreads) {
-          const int kc = idx / per_chunk;
-          const int rem = idx - kc * per_chunk;
-          const int nrow = rem >> 3;
-          const int j = (rem & 7) ^ (nrow & 7);
-          const int k = kc * kChunk + j * 8;
-          if (k < a.K) {
-            uint4* p = reinterpret_cast<uint4*>(w_smem + static_cast<size_t>(idx) * 16);
-            *p = scale_bf16x8(*p, __ldg(wts + k / a.r));
-          }
-        }
-        fence_proxy_async_smem();
-        named_sync(1, kEpiThreads);
-        if (et == 0) mbar_arrive(&bars->w_ready);
-      }
       float c2 = 0.0f, r2 = 0.0f;
       bool ok = true;
       for (int t = 0; t < x.ntiles; ++t) {
@@ -618,23 +665,48 @@ cudaError_t launch_d(const Dims& dm, const SegTable& seg, const View refv[2], co
   constexpr int REFB = kBM * D * 2;
   const size_t fixed = 1024 + sizeof(Bars) + 64;
   const size_t budget = static_cast<size_t>(di.max_smem_optin);
-  // Prefer three ref buffers (deferred store release) with >= 4 U stages,
-  // then two with >= 3, then one with >= 2.
-  int nrb = 0, nsu = 0;
-  const int want_nsu[4] = {0, 2, 3, 4};
-  for (int cand = kMaxRefBufs; cand >= 1; --cand) {
-    const size_t used = fixed + static_cast<size_t>(KC) * WCB + static_cast<size_t>(cand) * REFB;
+  // Shared memory: a ring of W chunk slots (at least one item's KC chunks;
+  // slots beyond KC let the next item's W load and fold early), the U ring
+  // and the ref/out tile buffers.  Candidates in order of preference, from a
+  // sweep on 512-token segments (K = A r = 256: two spare W chunks, two ref
+  // buffers and four U stages beat a full second W buffer with two U stages
+  // by 12%; K = 512: one spare chunk, one ref buffer, three U stages).
+  struct Cfg {
+    int extra_w, nrb, min_nsu;
+  };
+  const Cfg prefs[] = {{2, 2, 4}, {1, 2, 4}, {1, 1, 3}, {1, 1, 2}, {0, 1, 2}};
+  int nws = 0, nrb = 0, nsu = 0;
+#ifdef KVC_TUNING
+  if (const char* env = std::getenv("KVC_APPLY_CONFIG")) {   // "extra_w,nrb,nsu" (tuning builds)
+    int x = 0, b = 0, u = 0;
+    if (std::sscanf(env, "%d,%d,%d", &x, &b, &u) == 3 && x >= 0 && x <= KC && b >= 1 &&
+        b <= kMaxRefBufs && u >= 2 && u <= kMaxUStages && KC + x <= kMaxWSlots) {
+      const size_t used = fixed + static_cast<size_t>(KC + x) * WCB +
+                          static_cast<size_t>(b) * REFB + static_cast<size_t>(u) * kUStageBytes;
+      if (used <= budget) {
+        nws = KC + x;
+        nrb = b;
+        nsu = u;
+      }
+    }
+  }
+#endif
+  for (const Cfg& c : prefs) {
+    if (nws != 0) break;
+    const int w = KC + c.extra_w;
+    if (c.extra_w < 0 || w > kMaxWSlots) continue;
+    const size_t used = fixed + static_cast<size_t>(w) * WCB + static_cast<size_t>(c.nrb) * REFB;
     if (used >= budget) continue;
     int n = static_cast<int>((budget - used) / kUStageBytes);
     if (n > kMaxUStages) n = kMaxUStages;
-    if (n >= want_nsu[cand]) {
-      nrb = cand;
+    if (n >= c.min_nsu) {
+      nws = w;
+      nrb = c.nrb;
       nsu = n;
-      break;
     }
   }
-  if (nrb < 1 || nsu < 2) return cudaErrorInvalidConfiguration;
-  const size_t smem = fixed + static_cast<size_t>(KC) * WCB + static_cast<size_t>(nrb) * REFB +
+  if (nws < KC || nrb < 1 || nsu < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = fixed + static_cast<size_t>(nws) * WCB + static_cast<size_t>(nrb) * REFB +
                       static_cast<size_t>(nsu) * kUStageBytes;
 
   TcMaps maps;
@@ -705,6 +777,7 @@ cudaError_t launch_d(const Dims& dm, const SegTable& seg, const View refv[2], co
   a.n_items = static_cast<int32_t>(items);
   a.n_ustages = nsu;
   a.n_refbufs = nrb;
+  a.n_wslots = nws;
 
   e = cudaFuncSetAttribute(apply_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));

@@ -10,21 +10,31 @@ tokens corrected per edge (all layers, K and V) times edges, divided by the
 step time.  Inputs are far larger than the 129 MB L2 (several GB per edge), so
 no explicit L2 flush is needed between steps.
 
-Default workload: the Llama-3.1-8B-shaped 2K chain (32 layers x 8 KV heads x
-d 128, bf16, 10 requests x 2,048 shared tokens, 8 anchors, r = 32, tau 0.32,
-10% planted fallback).
+Default workload: the concurrent serving batch (Llama-3.1-8B KV shape: 32
+layers x 8 KV heads x d 128, bf16; 16 requests x 16 PH segments of 512 tokens
+behind 128-token agent-specific PF segments, 131,072 PH tokens per edge; 8
+anchors, r = 32, tau 0.32, 10% planted fallback; chain of 4 agents).  The
+chain alternates two output caches (the held cache of agent j - 1 and the
+output of agent j), so every agent's exact cache, every edge's anchor states
+and two outputs (~259 GB) are resident when the timed region starts.  The
+step time is the mean over the timed steps (CUDA events around all of them,
+after the warm-up steps).
 
 Prints ONE JSON line on rank 0: the headline metric, the apply kernel's
 roofline (algorithmic bytes over its CUDA-event time against the measured HBM
 copy peak, and the DRAM traffic of the committed ncu capture), clocks sampled
-during the timed region, the end-to-end number with host buffers (``e2e``),
-the oracle's CPU rate (``cpu_baseline``), and the fractions of the other
-steps: ``match`` (the mean-key match alone), ``edge`` (one whole edge),
-``builder`` (workloads that build states) and ``representation``
-(rank-r_C workloads).  Under torchrun every rank corrects its own batch
-(weak scaling); the time is the slowest rank's.  ``--impl reference`` times
-the fp64 CPU oracle instead (the only other place this file executes the
-oracle is the ``cpu_baseline`` leg).
+during the timed region, the end-to-end number with host buffers (``e2e``,
+with the pinned-copy link peak measured in the same run), the oracle's CPU
+rate on all host cores and on one (``cpu_baseline``), and the fractions of
+the other steps: ``match`` (the mean-key match alone), ``edge`` (one whole
+edge), ``builder`` (the state builder on the long-context shapes, 32,768
+matrices of 512 x 128, run after the main workload is freed) and
+``representation`` (rank-r_C workloads).  Fractions are given against the
+measured copy peak (read + write) and, for the read-mostly match, also
+against the nominal 7.9 TB/s.  Under torchrun every rank corrects its own
+batch (weak scaling); the time is the slowest rank's.  ``--impl reference``
+times the fp64 CPU oracle instead (the only other place this file executes
+the oracle is the ``cpu_baseline`` leg).
 """
 from __future__ import annotations
 
@@ -43,16 +53,19 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HBM_FALLBACK_GBS = 6800.0
+HBM_NOMINAL_GBS = 7900.0
+# pinned host memory the end-to-end leg may hold for its inputs
+E2E_HOST_BUDGET = 96 << 30
 KERNEL_SRC = os.path.join(ROOT, "agent_shared_context_gb300", "csrc", "kvc_apply_tc.cu")
 
 
 def _args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["kvc", "reference"], default="kvc")
-    p.add_argument("--workload", default="llama2k")
+    p.add_argument("--workload", default="concurrent")
     p.add_argument("--requests", type=int, default=0,
                    help="use only the first N requests of the workload (small profiling cases)")
     p.add_argument("--segments", type=int, default=0,
@@ -60,6 +73,9 @@ def _args():
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-builder-leg", action="store_true",
+                   help="skip the state-builder leg on the long-context shapes")
+    p.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     return p.parse_args()
 
 
@@ -186,42 +202,77 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- oracle arm
-def _oracle_sample(wl, seconds_hint: float = 20.0):
+def _oracle_sample(wl, target_s: float = 12.0):
     """Time the fp64 oracle on a bounded sample: the first request's first
-    segment, a prefix of its (layer, head) units, every edge.  Returns
-    (corrected tokens/s equivalent, description)."""
-    import numpy as np
+    segment over every edge, on as many of its layers (all heads) as fit about
+    ``target_s`` seconds (one layer is timed first to size the sample).
+    Returns (corrected tokens/s extrapolated to all layers, seconds of the
+    sized run, description)."""
     import oracle as O
     from agent_shared_context_gb300 import synth
-    s0 = 0
-    n = wl.seg_len[s0]
-    units_total = wl.L * wl.H
-    n_units = max(1, min(units_total, 16))
-    Lk = max(1, n_units // wl.H)
-    n_units = Lk * wl.H
-    sub = synth.scaled(wl, L=Lk, R=1, seg_len=[n], name=wl.name + "-oracle-sample")
-    inp = synth.generate(sub, device="cpu")
-    seg = O.Segments(sub.seg_request, sub.seg_start, sub.seg_len)
-    EK = [t.double().numpy() for t in inp.exact_K]
-    EV = [t.double().numpy() for t in inp.exact_V]
-    states = [O.States(*(x.double().numpy() for x in (e.U_K, e.W_K, e.U_V, e.W_V))) for e in inp.edges]
-    summ = [e.summaries.double().numpy() for e in inp.edges]
-    build = None
-    if sub.build_slot >= 0:
-        build = dict(slot=sub.build_slot, r=sub.r, omega=inp.omega.double().numpy(),
-                     q=sub.power_iters, frac=sub.energy_frac)
-    rep = None
-    if sub.summary_mode == "rank":
-        summ = [e.reps.double().numpy() for e in inp.edges]
-        rep = dict(r_c=sub.rank_c, omega=inp.omega_c.double().numpy(), q=sub.power_iters)
-    t0 = time.perf_counter()
-    O.chain(EK, EV, seg, states, summ, sub.k_top, sub.temperature, sub.tau, build=build, rep=rep)
-    dt = time.perf_counter() - t0
-    tokens = n * sub.edges * (n_units / units_total)
+    n = wl.seg_len[0]
+
+    def run(Lk):
+        sub = synth.scaled(wl, L=Lk, R=1, seg_len=[n], name=wl.name + "-oracle-sample")
+        inp = synth.generate(sub, device="cpu", context_free=False)
+        seg = O.Segments(sub.seg_request, sub.seg_start, sub.seg_len)
+        EK = [t.double().numpy() for t in inp.exact_K]
+        EV = [t.double().numpy() for t in inp.exact_V]
+        states = [O.States(*(x.double().numpy() for x in (e.U_K, e.W_K, e.U_V, e.W_V)))
+                  for e in inp.edges]
+        summ = [e.summaries.double().numpy() for e in inp.edges]
+        build = None
+        if sub.build_slot >= 0:
+            build = dict(slot=sub.build_slot, r=sub.r, omega=inp.omega.double().numpy(),
+                         q=sub.power_iters, frac=sub.energy_frac)
+        rep = None
+        if sub.summary_mode == "rank":
+            summ = [e.reps.double().numpy() for e in inp.edges]
+            rep = dict(r_c=sub.rank_c, omega=inp.omega_c.double().numpy(), q=sub.power_iters)
+        t0 = time.perf_counter()
+        O.chain(EK, EV, seg, states, summ, sub.k_top, sub.temperature, sub.tau, build=build,
+                rep=rep)
+        return time.perf_counter() - t0
+
+    dt = run(1)
+    Lk = 1
+    if dt < target_s and wl.L > 1:
+        Lk = int(min(wl.L, max(1, target_s // max(dt, 1e-3))))
+        if Lk > 1:
+            dt = run(Lk)
+    n_units, units_total = Lk * wl.H, wl.L * wl.H
+    tokens = n * wl.edges * (n_units / units_total)
     desc = ("oracle chain over %d edges of one %d-token segment, %d of %d (layer, head) "
-            "units (%d layers x %d heads); tokens scaled by %d/%d" %
-            (sub.edges, n, n_units, units_total, Lk, wl.H, n_units, units_total))
+            "units (%d layers x %d heads); tokens/s extrapolated linearly to all %d units "
+            "(x %d/%d)" % (wl.edges, n, n_units, units_total, Lk, wl.H, units_total,
+                           n_units, units_total))
     return tokens / dt, dt, desc
+
+
+def _oracle_one_thread(workload: str):
+    """The same oracle sample in a child process whose BLAS runs on one
+    thread (the thread count is fixed before numpy loads)."""
+    env = dict(os.environ)
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = "1"
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    try:
+        p = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample",
+                            "--workload", workload], env=env, capture_output=True, text=True,
+                           timeout=600)
+        return json.loads(p.stdout.strip().splitlines()[-1])
+    except Exception as exc:  # pragma: no cover - reported, not fatal
+        return {"error": str(exc)[:200]}
+
+
+def _cpu_baseline(wl):
+    v, dt, desc = _oracle_sample(wl)
+    one = _oracle_one_thread(wl.name)
+    return {"value": v, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": desc, "seconds": dt,
+            "one_thread": {"value": one.get("value"), "cores": 1, "seconds": one.get("seconds"),
+                           "error": one.get("error")}}
 
 
 def run_reference(args, wl):
@@ -229,15 +280,13 @@ def run_reference(args, wl):
     if rank != 0:
         return
     vals = []
-    for _ in range(max(args.warmup, 0)):
-        pass  # the oracle has no warm-up state; warm-up steps are not re-run
     secs = 0.0
     desc = ""
     for _ in range(max(args.steps, 1)):
         v, dt, desc = _oracle_sample(wl)
         vals.append(v)
         secs += dt
-        if secs > 120:
+        if secs > 90:
             break
     value = statistics.median(vals)
     line = {
@@ -279,7 +328,92 @@ def whole_job_value(tokens_per_step_per_rank: int, world: int, ms_step: float) -
 
 
 # ------------------------------------------------------------------ GPU arm
+def _apply_bytes(wl) -> int:
+    """Algorithmic bytes of one apply launch over every segment: ref rows
+    read, out rows written, U rows and W read, K and V."""
+    e = wl.elem_bytes
+    Kr = wl.A * wl.r
+    return sum(wl.L * wl.H * 2 * (2 * n * wl.d * e + n * Kr * e + Kr * wl.d * e)
+               for n in wl.seg_len)
+
+
+def _match_bytes(wl) -> int:
+    """Algorithmic bytes of the mean-key match: the keys of every PH row and
+    the anchor summaries, plus weights and best written."""
+    return (wl.ph_tokens * wl.L * wl.H * wl.d * wl.elem_bytes
+            + wl.S * wl.L * wl.H * wl.A * (wl.d + 1) * 4)
+
+
+def _builder_leg(args, dev, wl_name: str = "longctx"):
+    """kvc_build_states alone on one edge of a state-building workload (the
+    long-context shapes by default: 64 segments x 512 tokens x 32 layers x 8
+    heads, K and V = 32,768 matrices of 512 x 128, r = 32, p = 8, q = 2)."""
+    import torch
+    from agent_shared_context_gb300 import kvc, synth
+    wl = synth.workload(wl_name)
+    inp = synth.generate(wl, device=dev, edges=[1], context_free=False)
+    e = inp.edges[0]
+    seg = kvc.Segments.from_workload(wl)
+    prm = kvc.params_from_workload(wl)
+    S, L, H, l = wl.S, wl.L, wl.H, wl.l
+    sigma = torch.empty((S, L, H, 2, l), device=dev)
+    erank = torch.empty((S, L, H, 2), dtype=torch.int32, device=dev)
+    ws = torch.empty(max(kvc.kvc_build_states_workspace(seg, prm), 256), dtype=torch.uint8,
+                     device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    b_ms = _time_launches(torch, stream, lambda: kvc.kvc_build_states(
+        seg, prm, inp.exact_K[1], inp.exact_V[1], inp.exact_K[0], inp.exact_V[0], inp.omega,
+        wl.build_slot, e.U_K, e.W_K, e.U_V, e.W_V, sigma, erank, ws, st), n=5, warm=1)
+    if int(st.item()) != 0:
+        raise RuntimeError("builder device status %d" % int(st.item()))
+    mats = S * L * H * 2
+    eb = wl.elem_bytes
+    # GEMM flops of HMT Algorithm 4.4 with q power iterations (the products
+    # with delta and delta^T and the final U), per matrix
+    gemm_flop = sum(L * H * 2 * 2 * (2 * wl.power_iters + 2) * n * wl.d * l for n in wl.seg_len)
+    b_bytes = sum(L * H * 2 * (2 * n * wl.d * eb + (n + wl.d) * wl.r * eb) for n in wl.seg_len)
+    bf16_pk, bf16_kind = _bf16_peak()
+    peak, peak_kind = _peaks()
+    tflops = gemm_flop / (b_ms / 1000.0) / 1e12
+    b_gbs = b_bytes / (b_ms / 1000.0) / 1e9
+    tc = wl.d <= 128 and l <= 64
+    out = {"workload": wl.name, "kernel": "build_tc_kernel" if tc else "build_simt_kernel",
+           "launch_ms": b_ms, "matrices": mats, "matrix": "%d x %d" % (wl.max_seg_len, wl.d),
+           "hmt_gemm_equivalent_tflops": tflops,
+           "tensor_frac_of_bf16_peak": tflops / bf16_pk, "bf16_peak_tflops": bf16_pk,
+           "bf16_peak_kind": bf16_kind,
+           "algorithmic_bytes": b_bytes, "achieved_gbs": b_gbs, "hbm_frac": b_gbs / peak,
+           "hbm_peak_kind": peak_kind}
+    del inp, e, sigma, erank, ws
+    return out
+
+
+def _link_peak(torch, dev, nbytes: int = 4 << 30):
+    """Plain pinned-memory copies of nbytes each way (best of 3, CUDA events)."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    res = {}
+    for name, (dst, src) in (("h2d_gbs", (d, h)), ("d2h_gbs", (h, d))):
+        best = None
+        for _ in range(3):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            dst.copy_(src, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize(dev)
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        res[name] = nbytes / (best / 1000.0) / 1e9
+    res["bytes"] = nbytes
+    del h, d
+    return res
+
+
 def run_kvc(args, wl):
+    import gc
+
     import torch
     from agent_shared_context_gb300 import kvc, synth
     from agent_shared_context_gb300.chain import ChainRunner
@@ -297,8 +431,8 @@ def run_kvc(args, wl):
 
     # every rank corrects its own independent batch (weak scaling)
     wl_rank = rank_workload(wl, rank, world)
-    inp = synth.generate(wl_rank, device=dev)
-    runner = ChainRunner(wl_rank, inp, device=dev, use_dense=True)
+    inp = synth.generate(wl_rank, device=dev, context_free=False)
+    runner = ChainRunner(wl_rank, inp, device=dev, use_dense=True, keep_outputs=False)
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
@@ -337,39 +471,26 @@ def run_kvc(args, wl):
     part = torch.empty((wl.S, wl.L, wl.H, 4), device=dev)
     # as inside the chain: the apply also hands the next edge its key sums
     ksum = torch.empty((wl.S, wl.L, wl.H, 4, wl.d), device=dev) if runner.carry_ksum else None
-    n_rep = 10
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n_rep)]
-    for i in range(n_rep + 2):
-        if i >= 2:
-            evs[i - 2][0].record(stream)
-        kvc.kvc_apply_correction(seg, prm, inp.exact_K[0], inp.exact_V[0], e.U_K, e.W_K, e.U_V,
-                                 e.W_V, eo.weights, eo.out_K, eo.out_V, part, eo.score,
-                                 eo.fallback, runner.dev_status, ksum_out=ksum)
-        if i >= 2:
-            evs[i - 2][1].record(stream)
-    torch.cuda.synchronize(dev)
-    apply_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
-    ebytes = wl.elem_bytes
-    Kr = wl.A * wl.r
-    apply_bytes = 0
-    for s in range(wl.S):
-        n = wl.seg_len[s]
-        apply_bytes += wl.L * wl.H * 2 * (2 * n * wl.d * ebytes + n * Kr * ebytes + Kr * wl.d * ebytes)
+    apply_ms = _time_launches(torch, stream, lambda: kvc.kvc_apply_correction(
+        seg, prm, inp.exact_K[0], inp.exact_V[0], e.U_K, e.W_K, e.U_V, e.W_V, eo.weights,
+        eo.out_K, eo.out_V, part, eo.score, eo.fallback, runner.dev_status, ksum_out=ksum),
+        n=10, warm=2)
+    apply_bytes = _apply_bytes(wl)
     peak, peak_kind = _peaks()
     achieved = apply_bytes / (apply_ms / 1000.0) / 1e9
     traffic = _profile_traffic(wl.name)
 
     # ---- match alone (mean keys: the K_ref read) and one whole edge
     match = None
-    edge = None
-    match_bytes = wl.ph_tokens * wl.L * wl.H * wl.d * ebytes + wl.S * wl.L * wl.H * wl.A * (wl.d + 1) * 4
+    match_bytes = _match_bytes(wl)
     if not runner.rank_mode:
         m_ms = _time_launches(torch, stream, lambda: kvc.kvc_match_anchors(
             seg, prm, inp.exact_K[0], e.summaries, eo.weights, eo.best, None, runner.dev_status))
         m_gbs = match_bytes / (m_ms / 1000.0) / 1e9
-        match = {"kernel": "match_kernel", "launch_ms": m_ms, "algorithmic_bytes_per_launch": match_bytes,
-                 "achieved": m_gbs, "peak": peak, "unit": "GB/s", "frac": m_gbs / peak}
+        match = {"kernel": "match_kernel", "launch_ms": m_ms,
+                 "algorithmic_bytes_per_launch": match_bytes, "achieved": m_gbs, "unit": "GB/s",
+                 "peak": peak, "frac": m_gbs / peak, "peak_kind": peak_kind + " copy (read+write)",
+                 "nominal_hbm_gbs": HBM_NOMINAL_GBS, "frac_of_nominal": m_gbs / HBM_NOMINAL_GBS}
     e_ms = _time_launches(torch, stream, lambda: runner.run_edge(1), n=10)
     e_bytes = apply_bytes + (0 if runner.rank_mode else match_bytes)
     edge = {"what": "edge 1 through kvc_chain_edge (match from the keys, apply, reduce, fallback copy)"
@@ -378,67 +499,30 @@ def run_kvc(args, wl):
             "apply_plus_match_bytes": e_bytes,
             "frac_of_peak_over_apply_plus_match_bytes": e_bytes / (e_ms / 1000.0) / 1e9 / peak}
 
-    # ---- state builder (workloads that build anchor states), timed alone
-    builder = None
-    if runner.build:
-        eo1 = runner.edges[1]
-        evb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(3)]
-        for i in range(4):
-            if i >= 1:
-                evb[i - 1][0].record(stream)
-            kvc.kvc_build_states(seg, prm, inp.exact_K[1], inp.exact_V[1], inp.exact_K[0],
-                                 inp.exact_V[0], inp.omega, wl.build_slot, e.U_K, e.W_K, e.U_V,
-                                 e.W_V, eo1.sigma, eo1.eff_rank, runner.build_ws,
-                                 runner.dev_status)
-            if i >= 1:
-                evb[i - 1][1].record(stream)
-        torch.cuda.synchronize(dev)
-        b_ms = statistics.mean(a.elapsed_time(b) for a, b in evb)
-        mats = wl.S * wl.L * wl.H * 2
-        gemm_flop = 0
-        for s in range(wl.S):
-            gemm_flop += wl.L * wl.H * 2 * 2 * (2 * wl.power_iters + 2) * wl.seg_len[s] * wl.d * wl.l
-        tc = wl.d <= 128 and wl.l <= 64
-        # bytes the builder must move: exact and held rows read, U and W written
-        b_bytes = sum(wl.L * wl.H * 2 * (2 * n * wl.d * ebytes + (n + wl.d) * wl.r * ebytes)
-                      for n in wl.seg_len)
-        bf16_pk, bf16_kind = _bf16_peak()
-        tflops = gemm_flop / (b_ms / 1000.0) / 1e12
-        b_gbs = b_bytes / (b_ms / 1000.0) / 1e9
-        builder = {"kernel": "build_tc_kernel" if tc else "build_simt_kernel",
-                   "launch_ms": b_ms, "matrices": mats,
-                   "hmt_gemm_equivalent_tflops": tflops,
-                   "tensor_frac_of_bf16_peak": tflops / bf16_pk, "bf16_peak_tflops": bf16_pk,
-                   "bf16_peak_kind": bf16_kind,
-                   "algorithmic_bytes": b_bytes, "achieved_gbs": b_gbs, "hbm_frac": b_gbs / peak,
-                   "bound": "latency of the fp32 small-matrix steps (see profiles)",
-                   "tensor_path": ("M = delta^T delta on tcgen05 (split bf16)" if tc
-                                   else "FP32 FMA")}
-
     # ---- rank-r_C representations of the held keys (one launch per edge), timed alone
     representation = None
     if runner.rank_mode:
         qrep = torch.empty((wl.S, wl.L, wl.H, wl.d, wl.rank_c), device=dev)
-        evr = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(3)]
-        for i in range(4):
-            if i >= 1:
-                evr[i - 1][0].record(stream)
-            kvc.kvc_build_representation(seg, prm, inp.exact_K[0], qrep, None, None,
-                                         runner.dev_status)
-            if i >= 1:
-                evr[i - 1][1].record(stream)
-        torch.cuda.synchronize(dev)
-        r_ms = statistics.mean(a.elapsed_time(b) for a, b in evr)
+        r_ms = _time_launches(torch, stream, lambda: kvc.kvc_build_representation(
+            seg, prm, inp.exact_K[0], qrep, None, None, runner.dev_status), n=3, warm=1)
         representation = {"kernel": "build_tc_kernel (representation mode)", "launch_ms": r_ms,
                           "units": wl.S * wl.L * wl.H, "rank_c": wl.rank_c,
-                          "key_bytes_per_launch": wl.ph_tokens * wl.L * wl.H * wl.d * ebytes}
+                          "key_bytes_per_launch": wl.ph_tokens * wl.L * wl.H * wl.d * wl.elem_bytes}
+        del qrep
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e and world == 1:
         e2e = _e2e(args, wl, inp, runner, dev)
+
+    # ---- the state builder (its own workload, after the main one is freed)
+    builder = None
+    if world == 1 and not args.no_builder_leg:
+        build_name = wl.name if runner.build else "longctx"
+        del runner, inp, e, eo, part, ksum
+        gc.collect()
+        torch.cuda.empty_cache()
+        builder = _builder_leg(args, dev, build_name)
 
     line = {
         "metric": "corrected KV tokens/s (all layers, K+V)",
@@ -447,13 +531,17 @@ def run_kvc(args, wl):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
         "data": "synthetic",
         "config": {"workload": wl.name, "layers": wl.L, "kv_heads": wl.H, "head_dim": wl.d,
-                   "requests": wl.R, "ph_tokens_per_edge": wl.ph_tokens, "edges": wl.edges,
+                   "requests": wl.R, "ph_segments": wl.S, "segment_tokens": wl.max_seg_len,
+                   "ph_tokens_per_edge": wl.ph_tokens, "edges": wl.edges,
                    "anchors": wl.A, "rank": wl.r, "tau": wl.tau,
                    "l2": "inputs larger than L2 (no flush)",
+                   "timing": "mean over the timed steps, CUDA events around all of them",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "apply_tc_kernel", "peak_kind": peak_kind,
+                     "kernel": "apply_tc_kernel", "peak_kind": peak_kind + " copy (read+write)",
+                     "nominal_hbm_gbs": HBM_NOMINAL_GBS,
+                     "frac_of_nominal": achieved / HBM_NOMINAL_GBS,
                      "algorithmic_bytes_per_launch": apply_bytes, "launch_ms": apply_ms},
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
@@ -470,62 +558,93 @@ def run_kvc(args, wl):
         line["representation"] = representation
         line["config"]["summary"] = "rank-%d representations" % wl.rank_c
     if rank == 0 and not args.no_cpu_baseline:
-        v, dt, desc = _oracle_sample(wl)
-        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": _blas_threads(),
-                                "kind": "oracle", "sample": desc}
+        line["cpu_baseline"] = _cpu_baseline(wl)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
 
 
-def _e2e(args, wl, inp, runner, dev):
-    """Same chain through the C ABI, with every step's inputs copied from pinned
-    host memory and the last agent's corrected cache plus every edge's
-    scores/flags copied back, all inside the timed region."""
-    import torch
-    host_in = []
-    dev_in = []
-
-    def pin(t):
-        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-        h.copy_(t)
-        host_in.append(h)
-        dev_in.append(t)
-
-    pin(inp.exact_K[0])
-    pin(inp.exact_V[0])
+def _e2e_plan(wl, inp, runner):
+    """Inputs of one chain step (A0's cache; per edge the anchor states,
+    summaries and the dense caches) as (device tensor, axis kind) pairs:
+    'req' tensors are indexed by request on axis 0, 'seg' tensors by segment."""
+    items = [(inp.exact_K[0], "req"), (inp.exact_V[0], "req")]
     for j, e in enumerate(inp.edges, start=1):
         summaries = e.reps if runner.rank_mode else e.summaries
-        for t in (e.U_K, e.W_K, e.U_V, e.W_V, summaries, inp.exact_K[j], inp.exact_V[j]):
-            pin(t)
-    last = runner.edges[wl.edges]
-    outs = [last.out_K, last.out_V] + [runner.edges[j].score for j in range(1, wl.edges + 1)] + \
+        for t in (e.U_K, e.W_K, e.U_V, e.W_V, summaries):
+            items.append((t, "seg"))
+        items.append((inp.exact_K[j], "req"))
+        items.append((inp.exact_V[j], "req"))
+    return items
+
+
+def _e2e(args, wl, inp, runner, dev):
+    """The same chain through the C ABI, with every step's inputs copied from
+    pinned host memory and the last agent's corrected cache plus every edge's
+    scores and flags copied back, all inside the timed region.
+
+    When the inputs of the whole batch exceed the host budget (the concurrent
+    batch needs ~216 GB per step; the GPU machine has ~199 GB of host memory),
+    the host holds pinned buffers for one group of requests, and every step
+    uploads each request group of the batch from them (a group's rows and
+    segments are contiguous on the device): the bytes moved per step are the
+    whole batch's, but the request groups carry the same values.  The plain
+    pinned-copy bandwidth of the same box is measured beside it."""
+    import torch
+    items = _e2e_plan(wl, inp, runner)
+    seg_req = list(wl.seg_request)
+    assert seg_req == sorted(seg_req), "segments must be grouped by request"
+    total = sum(t.numel() * t.element_size() for t, _ in items)
+    per_req = total / wl.R
+    # largest divisor of R whose group fits the budget
+    g_req = 1
+    for gq in range(wl.R, 0, -1):
+        if wl.R % gq == 0 and gq * per_req <= E2E_HOST_BUDGET:
+            g_req = gq
+            break
+    groups = []
+    for g0 in range(0, wl.R, g_req):
+        segs = [s for s in range(wl.S) if g0 <= seg_req[s] < g0 + g_req]
+        groups.append(((g0, g0 + g_req), (segs[0], segs[-1] + 1)))
+    # host buffers hold group 0's values
+    (q0, q1), (s0, s1) = groups[0]
+    host_in = []
+    for t, kind in items:
+        src = t[q0:q1] if kind == "req" else t[s0:s1]
+        h = torch.empty(src.shape, dtype=src.dtype, pin_memory=True)
+        h.copy_(src)
+        host_in.append(h)
+    last_K, last_V = runner.held(wl.edges)
+    outs = [last_K, last_V] + [runner.edges[j].score for j in range(1, wl.edges + 1)] + \
            [runner.edges[j].fallback for j in range(1, wl.edges + 1)]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    copies = []                                   # (host buffer, device slice) per upload
+    for (qa, qb), (sa, sb) in groups:
+        for h, (t, kind) in zip(host_in, items):
+            copies.append((h, t[qa:qb] if kind == "req" else t[sa:sb]))
+    h2d = sum(h.numel() * h.element_size() for h, _ in copies)
     d2h = sum(h.numel() * h.element_size() for h in host_out)
     stream = torch.cuda.current_stream(dev)
     steps = max(1, args.e2e_steps)
     # the uploads are spread over several copy streams (largest first, to the
-    # least loaded stream) so that more than one copy engine moves data; the
-    # compute stream waits for all of them
+    # least loaded stream); the compute stream waits for all of them
     n_copy = 4
     copy_streams = [torch.cuda.Stream(dev) for _ in range(n_copy)]
-    order = sorted(range(len(host_in)), key=lambda i: -host_in[i].numel() * host_in[i].element_size())
+    order = sorted(range(len(copies)), key=lambda i: -copies[i][0].numel() * copies[i][0].element_size())
     load = [0] * n_copy
     assign = {}
     for i in order:
         k = min(range(n_copy), key=lambda c: load[c])
         assign[i] = k
-        load[k] += host_in[i].numel() * host_in[i].element_size()
+        load[k] += copies[i][0].numel() * copies[i][0].element_size()
 
     def step():
         ready = torch.cuda.Event()
         ready.record(stream)                     # the previous step's kernels are done with the inputs
         for cs in copy_streams:
             cs.wait_event(ready)
-        for i, (h, d) in enumerate(zip(host_in, dev_in)):
+        for i, (h, d) in enumerate(copies):
             with torch.cuda.stream(copy_streams[assign[i]]):
                 d.copy_(h, non_blocking=True)
         for cs in copy_streams:
@@ -546,15 +665,28 @@ def _e2e(args, wl, inp, runner, dev):
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / steps
+    del host_in, host_out, copies
+    link = _link_peak(torch, dev)
+    h2d_gbs = h2d / (ms / 1000.0) / 1e9
     return {"value": wl.ph_tokens * wl.edges / (ms / 1000.0), "unit": "tokens/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": ms, "steps": steps}
+            "ms_per_step": ms, "steps": steps,
+            "staging": ("whole batch" if len(groups) == 1 else
+                        "%d request groups of %d requests uploaded from one pinned group buffer "
+                        "(host memory cannot hold the batch's inputs)" % (len(groups), g_req)),
+            "h2d_achieved_gbs": h2d_gbs,
+            "link_peak": link,
+            "frac_of_h2d_link_peak": h2d_gbs / link["h2d_gbs"]}
 
 
 def main():
     args = _args()
     from agent_shared_context_gb300 import synth
     wl = synth.workload(args.workload)
+    if args.oracle_sample:
+        v, dt, desc = _oracle_sample(wl)
+        print(json.dumps({"value": v, "seconds": dt, "sample": desc}), flush=True)
+        return
     if 0 < args.requests < wl.R:
         import dataclasses
         keep = [s for s in range(wl.S) if wl.seg_request[s] < args.requests]

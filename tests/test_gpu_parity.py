@@ -5,12 +5,15 @@ the C ABI, and runs the oracle on the same input tensors (copied to the host
 and upcast exactly to float64).  Decisions must match exactly: fallback flags
 (the generator keeps segment scores >= 25% away from tau), and the best
 anchor and kept top-k set of every unit (the generator plants a similarity
-margin between the anchors' summaries; ``_harness.check_decisions`` checks
-every unit and requires 0 undecided ones except in the cases listed in
-``UNDECIDED_OK``, where segments of <= 24 tokens make the key mean large
-against the N(0, 0.1^2) summary perturbation, so the planted margins shrink
-below the threshold and any near-maximal anchor is a valid answer); floats
-follow the tolerances documented in ``tests/_harness.check_out``.
+margin between the anchors' summaries around the exact keys' mean;
+``_harness.check_decisions`` checks every unit and requires 0 undecided ones
+at edge 1 except in the cases listed in ``UNDECIDED_OK``, where segments of
+<= 24 tokens make the key mean large against the N(0, 0.1^2) summary
+perturbation, so the planted margins shrink below the threshold.  From edge 2
+on the query is the mean of the method's own corrected keys, which the
+generator cannot plant margins around: undecided units are counted and any
+near-maximal anchor is accepted there); floats follow the tolerances
+documented in ``tests/_harness.check_out``.
 """
 import math
 
@@ -128,8 +131,11 @@ def test_chain_matches_oracle(name):
         else:
             np.testing.assert_allclose(w_gpu, orc["weights"], rtol=1e-2, atol=1e-4)
             gap_min = 1e-3
+        # the planted margins hold for the generator's exact keys, i.e. at edge
+        # 1; from edge 2 on the query mean-pools the method's own corrected
+        # keys, so a near-tie is possible there and is checked for validity
         undecided = check_decisions(eo.best.cpu().numpy(), w_gpu, orc, summ[j - 1], wl.k_top,
-                                    gap_min, expect_decided=name not in UNDECIDED_OK)
+                                    gap_min, expect_decided=j == 1 and name not in UNDECIDED_OK)
         print("edge %d: undecided units %d of %d" % (j, undecided, wl.S * wl.L * wl.H))
         refK = res[j - 1]["out_K"]
         refV = res[j - 1]["out_V"]
