@@ -466,9 +466,10 @@ int64_t slot_floats(const Dims& dm, int l) {
 
 }  // namespace
 
-size_t build_workspace_bytes(const Dims& dm, int l) {
+size_t build_workspace_bytes(const Dims& dm, kvc_dtype dtype, int l) {
   const int64_t mats = dm.units() * 2;
   if (mats <= 0) return 0;
+  if (build_staged_supported(dm, dtype, l)) return build_staged_workspace_bytes(dm, l);
   if (build_tc_supported(dm, l)) return 0;      // the tensor-core builder keeps all on chip
   const int64_t slots = mats < kBuildSlots ? mats : kBuildSlots;
   return static_cast<size_t>(slots * slot_floats(dm, l) * static_cast<int64_t>(sizeof(float)));
@@ -480,6 +481,10 @@ cudaError_t launch_build(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
                          float* sigma, int32_t* eff_rank, void* workspace, int32_t* dev_status,
                          cudaStream_t stream, const uint8_t* seg_mask, const int32_t* seg_slot,
                          float* summaries) {
+  if (build_staged_supported(dm, dtype, l))
+    return launch_build_staged(dm, seg, exactv, refv, omega, l, q, energy_frac, slot, U, W,
+                               sigma, eff_rank, workspace, dev_status, stream, seg_mask,
+                               seg_slot, summaries);
   if (build_tc_supported(dm, l))
     return launch_build_tc(dm, seg, dtype, exactv, refv, omega, l, q, energy_frac, slot, U, W,
                            sigma, eff_rank, dev_status, stream, seg_mask, seg_slot, summaries);

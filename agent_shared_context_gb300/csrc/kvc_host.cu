@@ -321,7 +321,7 @@ const char* kvc_last_error(void) { return g_last_error; }
 size_t kvc_build_states_workspace(const kvc_segments* seg, const kvc_params* prm) {
   if (seg == nullptr || prm == nullptr) return 0;
   const Dims dm = make_dims(seg, prm);
-  return build_workspace_bytes(dm, prm->rank + prm->oversample);
+  return build_workspace_bytes(dm, seg->dtype, prm->rank + prm->oversample);
 }
 
 kvc_status kvc_build_states(const kvc_segments* seg, const kvc_params* prm,
@@ -349,7 +349,7 @@ kvc_status kvc_build_states(const kvc_segments* seg, const kvc_params* prm,
     return fail(KVC_ERR_INVALID_ARGUMENT, "slot %d outside [0, %d)", slot, prm->n_anchors);
   const Dims dm = make_dims(seg, prm);
   const int l = prm->rank + prm->oversample;
-  const size_t need = build_workspace_bytes(dm, l);
+  const size_t need = build_workspace_bytes(dm, seg->dtype, l);
   if (need > 0) {
     if (workspace == nullptr || workspace_bytes < need)
       return fail(KVC_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need,
@@ -396,7 +396,7 @@ kvc_status kvc_pool_insert(const kvc_segments* seg, const kvc_params* prm, kvc_c
   KVC_TRY(check_dev_ptr(dev_status, "dev_status"));
   const Dims dm = make_dims(seg, prm);
   const int l = prm->rank + prm->oversample;
-  const size_t need = build_workspace_bytes(dm, l);
+  const size_t need = build_workspace_bytes(dm, seg->dtype, l);
   if (need > 0) {
     if (workspace == nullptr || workspace_bytes < need)
       return fail(KVC_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need,

@@ -97,14 +97,28 @@ cudaError_t launch_fallback_copy(const Dims& dm, const SegTable& seg, kvc_dtype 
                                  const uint8_t* fallback, cudaStream_t stream,
                                  float* ksum = nullptr);
 
-// K1: randomized low-rank delta states.
-size_t build_workspace_bytes(const Dims& dm, int l);
+// K1: randomized low-rank delta states.  bf16 caches with d in {64, 128}
+// run the staged builder (kvc_build_staged.cu, workspace of one pass of up to
+// 8,192 matrices); f32 caches run the single-kernel builders.
+size_t build_workspace_bytes(const Dims& dm, kvc_dtype dtype, int l);
 cudaError_t launch_build(const Dims& dm, const SegTable& seg, kvc_dtype dtype,
                          const View exactv[2], const View refv[2], const float* omega, int l,
                          int q, float energy_frac, int slot, void* U[2], void* W[2],
                          float* sigma, int32_t* eff_rank, void* workspace, int32_t* dev_status,
                          cudaStream_t stream, const uint8_t* seg_mask = nullptr,
                          const int32_t* seg_slot = nullptr, float* summaries = nullptr);
+
+// K1 as a staged pipeline for bf16 caches (Gram on tcgen05, the small
+// factorisations one matrix per warp, the feature-row products per CTA).
+bool build_staged_supported(const Dims& dm, kvc_dtype dtype, int l);
+size_t build_staged_workspace_bytes(const Dims& dm, int l);
+cudaError_t launch_build_staged(const Dims& dm, const SegTable& seg, const View exactv[2],
+                                const View refv[2], const float* omega, int l, int q,
+                                float energy_frac, int slot, void* U[2], void* W[2],
+                                float* sigma, int32_t* eff_rank, void* workspace,
+                                int32_t* dev_status, cudaStream_t stream,
+                                const uint8_t* seg_mask, const int32_t* seg_slot,
+                                float* summaries);
 
 // K1 on tcgen05 (d <= 128, l <= 64): M = delta^T delta on tensor cores, the
 // subspace iteration on the feature side; needs no workspace.

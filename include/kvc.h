@@ -190,7 +190,11 @@ const char* kvc_last_error(void);
  * into sigma and the effective rank (fraction energy_frac of |delta|_F^2)
  * into eff_rank.  Every segment needs len >= l.  Other slots are untouched.
  * `workspace` must hold kvc_build_states_workspace() bytes (256-byte
- * aligned); it may be NULL when that size is 0.
+ * aligned); it may be NULL when that size is 0.  bf16 caches (d = 64 or 128)
+ * are factored in passes of up to 8,192 matrices (one (segment, layer, head,
+ * K|V) block each) and the workspace holds one pass: per matrix the d x d
+ * Gram of the delta, the d x l iterates and the l x l factors (about 180 KB
+ * at d = 128, l = 40; about 1.5 GB for a full pass).
  * ------------------------------------------------------------------------- */
 size_t kvc_build_states_workspace(const kvc_segments* seg, const kvc_params* prm);
 kvc_status kvc_build_states(const kvc_segments* seg, const kvc_params* prm,
