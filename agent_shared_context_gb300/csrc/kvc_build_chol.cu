@@ -1,0 +1,386 @@
+// kvc_build_chol.cu -- the l x l stages of the staged bf16 state builder
+// (kvc_build_staged.cu), one matrix per warp.
+//
+// A warp keeps its matrices column-major in shared memory with an odd column
+// stride cs: lane k owns columns k and k + 32, so the lanes of a warp touch
+// distinct banks when each updates its own column, and read the same address
+// (a broadcast) when they all need an entry of another column.  Loops are
+// compact (the step index runs at run time), which keeps the code small
+// enough to stay in the instruction cache with many warps resident.
+//
+//   chol_kernel<false>  T = R^-1, R the Cholesky factor of G (with dependent-
+//                       column dropping);
+//   chol_kernel<true>   CholeskyQR2 of the implicit iterate whose Gram is G:
+//                       T = R1^-1 R2^-1 with R2 from R1^-T G R1^-1;
+//   eig_kernel          eigenpairs of G = B B^T by one-sided (Hestenes)
+//                       Jacobi on the columns of R^T, R the Cholesky factor.
+#include "kvc_build_staged.cuh"
+
+namespace kvc {
+namespace staged {
+namespace {
+
+// Per-warp shared arrays of the l x l kernels.
+struct WarpMats {
+  float* A;        // column-major scratch (cs x l)
+  float* B;        // column-major scratch (cs x l)
+  float* C;        // column-major scratch (cs x l)
+  int* keep;       // [kLmax]
+  float* dinv;     // [kLmax]
+  float* diag;     // [kLmax]
+  float* lam;      // [kLmax]
+  int* order;      // [kLmax]
+};
+
+__device__ __forceinline__ int col_stride(int l) { return l | 1; }
+
+__device__ __forceinline__ size_t warp_floats(int l, int nmats) {
+  return static_cast<size_t>(nmats) * col_stride(l) * l + 5 * kLmax;
+}
+
+__device__ __forceinline__ WarpMats warp_mats(float* sh, int warp, int l, int nmats) {
+  const int cs = col_stride(l);
+  float* base = sh + warp * warp_floats(l, nmats);
+  WarpMats w;
+  w.A = base;
+  w.B = nmats > 1 ? base + cs * l : nullptr;
+  w.C = nmats > 2 ? base + 2 * cs * l : nullptr;
+  w.keep = reinterpret_cast<int*>(base + nmats * cs * l);
+  w.dinv = reinterpret_cast<float*>(w.keep + kLmax);
+  w.diag = w.dinv + kLmax;
+  w.lam = w.diag + kLmax;
+  w.order = reinterpret_cast<int*>(w.lam + kLmax);
+  return w;
+}
+
+// Cholesky G = R^T R (G symmetric, column-major, stride cs; R written
+// column-major into R, upper triangle): right-looking with the unscaled pivot
+// row, R[i][k] -= R[j][i] R[j][k] / pivot_j, rows scaled by dinv at the end;
+// a pivot below 1e-6 of its column's squared norm marks a dependent column
+// (keep[j] = 0, row j zero).  diag gets the final R[i][i].
+__device__ void chol_cols(const float* __restrict__ G, float* __restrict__ R, int* keep,
+                          float* dinv, float* diag, int l, int cs, int lane) {
+  for (int k = lane; k < l; k += 32)
+    for (int m = 0; m < l; ++m) R[k * cs + m] = m <= k ? G[k * cs + m] : 0.0f;
+  __syncwarp();
+  for (int j = 0; j < l; ++j) {
+    const float gjj = G[j * cs + j];
+    const float piv = R[j * cs + j];
+    const bool ok = gjj > 0.0f && piv > 1e-6f * gjj;
+    const float inv2 = ok ? 1.0f / piv : 0.0f;
+    if (lane == 0) {
+      keep[j] = ok ? 1 : 0;
+      dinv[j] = ok ? rsqrtf(piv) : 0.0f;
+    }
+    for (int k = lane; k < l; k += 32) {
+      if (k <= j) continue;
+      float* rk = R + k * cs;
+      const float rjk = rk[j];
+      int i = j + 1;
+      // eight rows at a time: every load issued before the stores (the row-j
+      // entries of other columns are not written in this step)
+      for (; i + 8 <= k + 1; i += 8) {
+        float t[8], v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          t[u] = R[(i + u) * cs + j];
+          v[u] = rk[i + u];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) rk[i + u] = fmaf(-t[u] * inv2, rjk, v[u]);
+      }
+      for (; i <= k; ++i) rk[i] = fmaf(-R[i * cs + j] * inv2, rjk, rk[i]);
+    }
+    __syncwarp();
+  }
+  for (int k = lane; k < l; k += 32) {
+    float* rk = R + k * cs;
+    for (int m = 0; m <= k; ++m) rk[m] *= dinv[m];
+    diag[k] = rk[k];
+  }
+  __syncwarp();
+}
+
+// Ri = R^-1 (column-major, upper triangle, stride cs) of the upper-
+// triangular R of chol_cols: back substitution from the last row up,
+// Ri[m][k] -= R[m][i] Ri[i][k] / R[i][i] for m < i <= k, rows scaled at the
+// end; dropped indices stay zero.  Entries below the diagonal are zero.
+__device__ void tri_inv_cols(const float* __restrict__ R, const int* keep, const float* diag,
+                             float* __restrict__ Ri, int l, int cs, int lane) {
+  for (int k = lane; k < l; k += 32)
+    for (int m = 0; m < l; ++m) Ri[k * cs + m] = (m == k && keep[m]) ? 1.0f : 0.0f;
+  __syncwarp();
+  for (int i = l - 1; i > 0; --i) {
+    const float inv = keep[i] ? 1.0f / diag[i] : 0.0f;
+    const float* ri = R + i * cs;
+    for (int k = lane; k < l; k += 32) {
+      if (k < i) continue;
+      float* ck = Ri + k * cs;
+      const float xi = ck[i] * inv;
+      int m = 0;
+      for (; m + 8 <= i; m += 8) {
+        float t[8], v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          t[u] = ri[m + u];
+          v[u] = ck[m + u];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ck[m + u] = fmaf(-t[u], xi, v[u]);
+      }
+      for (; m < i; ++m) ck[m] = fmaf(-ri[m], xi, ck[m]);
+    }
+    __syncwarp();
+  }
+  for (int k = lane; k < l; k += 32)
+    for (int m = 0; m < l; ++m) Ri[k * cs + m] *= keep[m] ? 1.0f / diag[m] : 0.0f;
+  __syncwarp();
+}
+
+// C = op(A) B, column-major l x l (stride cs), op(A) = A or A^T; lane k
+// computes its columns, t ascending.
+__device__ void cmm(const float* __restrict__ A, bool transA, const float* __restrict__ B,
+                    float* __restrict__ C, int l, int cs, int lane) {
+  for (int k = lane; k < l; k += 32) {
+    const float* bk = B + k * cs;
+    for (int m = 0; m < l; ++m) {
+      float acc = 0.0f;
+      if (transA) {
+        const float* am = A + m * cs;              // column m of A = row m of A^T
+#pragma unroll 4
+        for (int t = 0; t < l; ++t) acc = fmaf(am[t], bk[t], acc);
+      } else {
+#pragma unroll 4
+        for (int t = 0; t < l; ++t) acc = fmaf(A[t * cs + m], bk[t], acc);
+      }
+      C[k * cs + m] = acc;
+    }
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void load_gram(const float* Gg, float* G, int l, int lp, int cs,
+                                          int lane) {
+  // G is symmetric: row r of the global matrix is column r
+  for (int idx = lane; idx < l * l; idx += 32) {
+    const int r = idx / l, c = idx - (idx / l) * l;
+    G[r * cs + c] = Gg[r * lp + c];
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void store_cols(const float* M, float* Tg, int l, int lp, int cs,
+                                           int lane) {
+  // row-major global lp x lp, zero outside l x l
+  for (int idx = lane; idx < lp * lp; idx += 32) {
+    const int r = idx / lp, c = idx - (idx / lp) * lp;
+    Tg[idx] = (r < l && c < l) ? M[c * cs + r] : 0.0f;
+  }
+}
+
+template <bool kQr2>
+__global__ void __launch_bounds__(kSmallWarps * 32)
+    chol_kernel(const StageArgs a, const __grid_constant__ SegTable seg) {
+  const int l = a.l, lp = a.lp, cs = col_stride(l);
+  extern __shared__ float sh[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WarpMats w = warp_mats(sh, warp, l, kQr2 ? 3 : 2);
+  const int i = blockIdx.x * kSmallWarps + warp;
+  if (i >= a.nm) return;
+  const Mat x = decode_mat(a, seg, a.m0 + i);
+  if (x.skip) return;
+  load_gram(a.G + static_cast<int64_t>(i) * lp * lp, w.A, l, lp, cs, lane);
+  chol_cols(w.A, w.B, w.keep, w.dinv, w.diag, l, cs, lane);       // R in B
+  float* ri1 = kQr2 ? w.C : w.A;                                  // G is needed again for QR2
+  tri_inv_cols(w.B, w.keep, w.diag, ri1, l, cs, lane);
+  const float* out = ri1;
+  if (kQr2) {
+    cmm(w.A, false, w.C, w.B, l, cs, lane);                       // H = G Ri1      (B)
+    cmm(w.C, true, w.B, w.A, l, cs, lane);                        // G2 = Ri1^T H   (A)
+    chol_cols(w.A, w.B, w.keep, w.dinv, w.diag, l, cs, lane);     // R2             (B)
+    float* ri2 = w.A;                                             // G2 no longer needed
+    tri_inv_cols(w.B, w.keep, w.diag, ri2, l, cs, lane);          // Ri2            (A)
+    cmm(w.C, false, ri2, w.B, l, cs, lane);                       // R_Y^-1 = Ri1 Ri2 (B)
+    out = w.B;
+  }
+  store_cols(out, a.T + static_cast<int64_t>(i) * lp * lp, l, lp, cs, lane);
+}
+
+// Eigen-decomposition of the l x l Gram G = B B^T through its Cholesky factor
+// G = R^T R: one-sided (Hestenes) Jacobi orthogonalises the columns of
+// X = R^T by plane rotations, X J = Y, so that G = X X^T = Y Y^T =
+// sum_i |y_i|^2 (y_i / |y_i|)(y_i / |y_i|)^T: the eigenvalues are the squared
+// column norms and the eigenvectors the normalised columns, with no rotation
+// accumulator.  Column p of X (row p of R) is read with stride cs from the
+// column-major R.  Round-robin pairing, one pair per lane; a pair is rotated
+// while |y_p . y_q| > max(1e-7 |y_p| |y_q|, 2e-7 max_i |y_i|^2), and the
+// sweeps stop after one that rotates nothing.  Writes Ub (columns sorted by
+// descending eigenvalue), lam and the sigma / eff_rank outputs.
+__global__ void __launch_bounds__(kSmallWarps * 32)
+    eig_kernel(const StageArgs a, const __grid_constant__ SegTable seg) {
+  const int l = a.l, lp = a.lp, cs = col_stride(l);
+  const int n = (l + 1) & ~1;
+  const int np = n / 2;
+  extern __shared__ float sh[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WarpMats w = warp_mats(sh, warp, l, 2);
+  const int i = blockIdx.x * kSmallWarps + warp;
+  if (i >= a.nm) return;
+  const Mat x = decode_mat(a, seg, a.m0 + i);
+  if (x.skip) return;
+  load_gram(a.G + static_cast<int64_t>(i) * lp * lp, w.A, l, lp, cs, lane);
+  chol_cols(w.A, w.B, w.keep, w.dinv, w.diag, l, cs, lane);
+  float* Y = w.B;                 // y_p[e] = R[p][e] = Y[e * cs + p]
+  for (int sweep = 0; sweep < kSweepsOneSided; ++sweep) {
+    float nmax = 0.0f;
+    for (int p = lane; p < l; p += 32) {
+      float s2 = 0.0f;
+      for (int e = 0; e < l; ++e) s2 = fmaf(Y[e * cs + p], Y[e * cs + p], s2);
+      nmax = fmaxf(nmax, s2);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nmax = fmaxf(nmax, __shfl_xor_sync(0xffffffffu, nmax, o));
+    const float abs_tol = 2e-7f * nmax;
+    int rotated = 0;
+    for (int round = 0; round < n - 1; ++round) {
+      if (lane < np) {
+        const int k = lane;
+        int pa, pb;
+        if (k == 0) {
+          pa = n - 1;
+          pb = round;
+        } else {
+          pa = (round + k) % (n - 1);
+          pb = (round - k + (n - 1)) % (n - 1);
+        }
+        if (pa > pb) {
+          const int t = pa;
+          pa = pb;
+          pb = t;
+        }
+        if (pb < l) {
+          float app = 0.0f, aqq = 0.0f, apq = 0.0f;
+#pragma unroll 4
+          for (int e = 0; e < l; ++e) {
+            const float u = Y[e * cs + pa], v = Y[e * cs + pb];
+            app = fmaf(u, u, app);
+            aqq = fmaf(v, v, aqq);
+            apq = fmaf(u, v, apq);
+          }
+          const float tol = fmaxf(1e-7f * sqrtf(app * aqq), abs_tol);
+          if (fabsf(apq) > tol) {
+            const float theta = (aqq - app) / (2.0f * apq);
+            const float tt = copysignf(1.0f, theta) / (fabsf(theta) + sqrtf(theta * theta + 1.0f));
+            const float c = rsqrtf(tt * tt + 1.0f);
+            const float sn = tt * c;
+            int e = 0;
+            for (; e + 8 <= l; e += 8) {
+              float u[8], v[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                u[q] = Y[(e + q) * cs + pa];
+                v[q] = Y[(e + q) * cs + pb];
+              }
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                Y[(e + q) * cs + pa] = c * u[q] - sn * v[q];
+                Y[(e + q) * cs + pb] = sn * u[q] + c * v[q];
+              }
+            }
+            for (; e < l; ++e) {
+              const float u = Y[e * cs + pa], v = Y[e * cs + pb];
+              Y[e * cs + pa] = c * u - sn * v;
+              Y[e * cs + pb] = sn * u + c * v;
+            }
+            rotated = 1;
+          }
+        }
+      }
+      __syncwarp();
+    }
+    if (!__any_sync(0xffffffffu, rotated)) break;
+  }
+  // eigenvalues |y_p|^2, descending order (ties to the lower index)
+  for (int p = lane; p < l; p += 32) {
+    float s2 = 0.0f;
+    for (int e = 0; e < l; ++e) s2 = fmaf(Y[e * cs + p], Y[e * cs + p], s2);
+    w.lam[p] = s2;
+  }
+  __syncwarp();
+  for (int p = lane; p < l; p += 32) {
+    int rank = 0;
+    for (int k = 0; k < l; ++k)
+      rank += (w.lam[k] > w.lam[p] || (w.lam[k] == w.lam[p] && k < p)) ? 1 : 0;
+    w.order[rank] = p;
+  }
+  __syncwarp();
+  float* Ubg = a.Ub + static_cast<int64_t>(i) * lp * lp;
+  for (int idx = lane; idx < lp * lp; idx += 32) {
+    const int r = idx / lp, j = idx - (idx / lp) * lp;
+    float v = 0.0f;
+    if (r < l && j < l) {
+      const int src = w.order[j];
+      const float nrm = w.lam[src];
+      v = nrm > 0.0f ? Y[r * cs + src] * rsqrtf(nrm) : 0.0f;
+    }
+    Ubg[idx] = v;
+  }
+  float* lg = a.lam + static_cast<int64_t>(i) * lp;
+  for (int j = lane; j < lp; j += 32) lg[j] = j < l ? w.lam[w.order[j]] : 0.0f;
+  if (lane == 0) {
+    const int64_t mi = static_cast<int64_t>(x.unit) * 2 + x.kv;
+    const float total = a.ss[i];
+    float* sg = a.sigma != nullptr ? a.sigma + mi * l : nullptr;
+    float cum = 0.0f;
+    int er = l + 1;
+    const float target = a.energy_frac * total;
+    for (int k = 0; k < l; ++k) {
+      const float lk = w.lam[w.order[k]];
+      if (sg != nullptr) sg[k] = sqrtf(lk);
+      cum += lk;
+      if (er == l + 1 && cum >= target) er = k + 1;
+    }
+    if (!(total > 0.0f)) er = 0;
+    if (a.eff_rank != nullptr) a.eff_rank[mi] = er;
+  }
+}
+
+size_t smem_bytes(int l, int nmats) {
+  return static_cast<size_t>(kSmallWarps) *
+         (static_cast<size_t>(nmats) * (l | 1) * l + 5 * kLmax) * sizeof(float);
+}
+
+}  // namespace
+
+size_t chol_smem_bytes(bool qr2, int l) { return smem_bytes(l, qr2 ? 3 : 2); }
+size_t eig_smem_bytes(int l) { return smem_bytes(l, 2); }
+
+cudaError_t launch_chol(const StageArgs& a, const SegTable& seg, bool qr2, int grid, size_t smem,
+                        cudaStream_t stream) {
+  const int threads = kSmallWarps * 32;
+  cudaError_t e;
+  if (qr2) {
+    if ((e = cudaFuncSetAttribute(chol_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(smem))) != cudaSuccess)
+      return e;
+    chol_kernel<true><<<grid, threads, smem, stream>>>(a, seg);
+  } else {
+    if ((e = cudaFuncSetAttribute(chol_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(smem))) != cudaSuccess)
+      return e;
+    chol_kernel<false><<<grid, threads, smem, stream>>>(a, seg);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_eig(const StageArgs& a, const SegTable& seg, int grid, size_t smem,
+                       cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  eig_kernel<<<grid, kSmallWarps * 32, smem, stream>>>(a, seg);
+  return cudaGetLastError();
+}
+
+}  // namespace staged
+}  // namespace kvc

@@ -23,95 +23,37 @@
 //   chol_kernel    (warp = matrix) Cholesky with dependent-column dropping and
 //                  the triangular inverse: R^-1 of G, or R_Y^-1 of CholeskyQR2;
 //   zg_kernel      (thread = feature row) Z = P1 R^-1 and its Gram Z^T Z;
-//   jacobi_kernel  (warp = matrix) parallel cyclic Jacobi of B B^T = Z^T Z,
-//                  eigenpairs sorted, sigma and the effective rank;
+//   eig_kernel     (warp = matrix) eigenpairs of B B^T = Z^T Z by one-sided
+//                  Jacobi on the columns of R^T, R its Cholesky factor;
+//                  sorted, with sigma and the effective rank;
 //   wp_kernel      (thread = feature row) W = Z Ub_r Sigma_r^-1 (output) and
 //                  P = X R_Y^-1 Ub_r Sigma_r (workspace);
-//   u_kernel       (thread = token row) U = delta P, rows past the segment
+//   u_kernel       U = delta P from 64-row tiles of the exact and reference
+//                  rows (cp.async, two stages), rows past the segment
 //                  zeroed; for pool insertion the held-key mean.
 //
-// Every per-element operation (summation orders included) matches the
-// single-kernel builder, so both give the same states; the small l x l steps
-// run one matrix per warp with warp-level synchronisation only, so a CTA of
-// four warps keeps four of them in flight.  The only wait is the Gram
-// kernel's MMA completion, bounded by kWaitLimitNs.
+// The Gram, the products and the Cholesky / triangular-inverse steps match
+// the single-kernel builder element for element (summation orders included);
+// the final l x l eigenproblem uses one-sided Jacobi on the Cholesky factor
+// (same eigenpairs up to rounding and signs, which U W^T does not see).  The
+// small l x l steps run one matrix per warp -- columns in registers,
+// warp-level synchronisation only -- so a CTA of four warps keeps four of
+// them in flight.  The only wait is the Gram kernel's MMA completion, bounded
+// by kWaitLimitNs.
 #include <cuda_bf16.h>
 
 #include <algorithm>
 
-#include "kvc_internal.h"
+#include "kvc_build_staged.cuh"
 #include "kvc_ptx.cuh"
 
 namespace kvc {
 namespace {
 
 using namespace ptx;
+using namespace staged;
 
-constexpr int kGramThreads = 256;
-constexpr int kDP = 128;                  // feature rows of the Gram MMA (d padded)
-constexpr int kTok = 64;                  // tokens per delta^T chunk (MMA K)
-constexpr int kLmax = 64;
-constexpr int kSweeps = 14;
-constexpr int kRowThreads = 128;          // feature-row kernels
-constexpr int kSmallWarps = 4;            // l x l kernels: one matrix per warp
-constexpr int kUThreads = 256;
-constexpr int kPassMats = 8192;           // matrices per pass through the stages
-constexpr uint32_t kGramCols = 128;
 constexpr uint32_t kIdescM = idesc_bf16_f32(128, 128);
-
-struct StageArgs {
-  const char* exact[2];
-  const char* ref[2];
-  int64_t es[2][4];          // exact strides (req, layer, head, tok), elements
-  int64_t rs[2][4];
-  const float* omega;        // [d, l]
-  char* U[2];                // [S, L, H, Tmax, A, r] bf16
-  char* W[2];                // [S, L, H, d, A, r] bf16
-  float* sigma;              // [S, L, H, 2, l]
-  int32_t* eff_rank;         // [S, L, H, 2]
-  float* summaries;          // pool insertion: [S, L, H, A, d] (else nullptr)
-  const uint8_t* seg_mask;   // pool insertion: build only flagged segments
-  const int32_t* seg_slot;   // pool insertion: slot = seg_slot[s] mod A
-  int32_t* dev_status;
-  int32_t L, H, d, Tmax, A, r, l, lp, slot;
-  float energy_frac;
-  int32_t m0, nm;            // matrices [m0, m0 + nm) of this pass
-  // workspace of the pass, indexed by matrix - m0
-  float* M;                  // [nm, d, d]: M[i][k][c] = (delta^T delta)(c, k)
-  float* ss;                 // [nm] |delta|_F^2
-  float* X;                  // [nm, d, lp]
-  float* P1;                 // [nm, d, lp]
-  float* Z;                  // [nm, d, lp]
-  float* G;                  // [nm, lp, lp]
-  float* T;                  // [nm, lp, lp]
-  float* Ub;                 // [nm, lp, lp] eigenvectors, columns sorted
-  float* lam;                // [nm, lp]     eigenvalues, sorted descending
-  float* P;                  // [nm, d, r]
-};
-
-struct Mat {
-  int unit, kv, s, lyr, h, n, slot;
-  bool skip;
-};
-
-__device__ __forceinline__ Mat decode_mat(const StageArgs& a, const SegTable& seg, int m) {
-  Mat x;
-  x.kv = m & 1;
-  x.unit = m >> 1;
-  x.h = x.unit % a.H;
-  x.lyr = (x.unit / a.H) % a.L;
-  x.s = x.unit / (a.H * a.L);
-  x.n = seg.len[x.s];
-  x.skip = a.seg_mask != nullptr && a.seg_mask[x.s] == 0;
-  x.slot = a.seg_slot != nullptr ? ((a.seg_slot[x.s] % a.A) + a.A) % a.A : a.slot;
-  return x;
-}
-
-__device__ __forceinline__ const __nv_bfloat16* rows_of(const char* base, const int64_t* st,
-                                                        const SegTable& seg, const Mat& x) {
-  return reinterpret_cast<const __nv_bfloat16*>(base) + seg.req[x.s] * st[0] + x.lyr * st[1] +
-         x.h * st[2] + static_cast<int64_t>(seg.start[x.s]) * st[3];
-}
 
 // =================================================================== Gram
 // Thread = (4 adjacent features, 8 tokens) of a 64-token chunk: eight 8-byte
@@ -209,7 +151,8 @@ __global__ void __launch_bounds__(kGramThreads, 3)
     for (int kc = 0; kc < nchunks; ++kc) {
       const int b = kc & 1;
       if (pending[b]) {                                     // the MMAs of chunk kc - 2 read it
-        const bool got = mbar_wait_bounded(&mbar[b], ph[b], kWaitLimitNs);
+        // one thread polls (bounded), the barrier publishes the outcome
+        const bool got = threadIdx.x != 0 || mbar_wait_bounded(&mbar[b], ph[b], kWaitLimitNs);
         ph[b] ^= 1u;
         pending[b] = false;
         if (!__syncthreads_and(got)) {
@@ -243,7 +186,7 @@ __global__ void __launch_bounds__(kGramThreads, 3)
     bool got = true;
     for (int b = 0; b < 2; ++b) {
       if (pending[b]) {
-        got &= mbar_wait_bounded(&mbar[b], ph[b], kWaitLimitNs);
+        if (threadIdx.x == 0) got &= mbar_wait_bounded(&mbar[b], ph[b], kWaitLimitNs);
         ph[b] ^= 1u;
         pending[b] = false;
       }
@@ -331,29 +274,69 @@ __device__ __forceinline__ void gram_blocks(const float* As, const float* Bs, fl
   }
 }
 
-// Row c of a d x lp matrix times an lp x lp shared matrix Ts (stride lp):
-// out[j] = sum_{t < l} in[t] Ts[t][j], t ascending.
-__device__ __forceinline__ void row_times(const float* in, const float* Ts, float* out, int l,
+// The d x l iterates live in the workspace transposed ([lp][d], entry (c, j)
+// at j * d + c), so the threads of a CTA (thread = feature row c) read and
+// write them coalesced.  A row times an lp x lp matrix runs over t at run
+// time with the lp accumulators in registers (static indices) and the matrix
+// read from shared memory as broadcasts.
+struct RowAcc {
+  float4 v[kLmax / 4];
+};
+
+__device__ __forceinline__ void row_zero(RowAcc& r) {
+#pragma unroll
+  for (int q4 = 0; q4 < kLmax / 4; ++q4) r.v[q4] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+}
+
+// acc[j] += sum_{t < l} inT[t * d + c] Ts[t][j] (t ascending); Ts stride lp.
+__device__ __forceinline__ void row_times(const float* inT, int d, int c, const float* Ts,
+                                          RowAcc& acc, int l, int lp) {
+#pragma unroll 4
+  for (int t = 0; t < l; ++t) {
+    const float v = inT[static_cast<int64_t>(t) * d + c];
+    const float* tr = Ts + t * lp;
+#pragma unroll
+    for (int q4 = 0; q4 < kLmax / 4; ++q4) {
+      if (4 * q4 < lp) {
+        const float4 b = *reinterpret_cast<const float4*>(tr + 4 * q4);
+        acc.v[q4].x = fmaf(v, b.x, acc.v[q4].x);
+        acc.v[q4].y = fmaf(v, b.y, acc.v[q4].y);
+        acc.v[q4].z = fmaf(v, b.z, acc.v[q4].z);
+        acc.v[q4].w = fmaf(v, b.w, acc.v[q4].w);
+      }
+    }
+  }
+}
+
+// Store a row to shared memory (row-major, stride lp) and to the transposed
+// global array.
+__device__ __forceinline__ void row_store(const RowAcc& acc, float* rs, float* gT, int d, int c,
                                           int lp) {
 #pragma unroll
   for (int q4 = 0; q4 < kLmax / 4; ++q4) {
     if (4 * q4 < lp) {
-      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      for (int t = 0; t < l; ++t) {
-        const float4 b = *reinterpret_cast<const float4*>(Ts + t * lp + 4 * q4);
-        acc.x = fmaf(in[t], b.x, acc.x);
-        acc.y = fmaf(in[t], b.y, acc.y);
-        acc.z = fmaf(in[t], b.z, acc.z);
-        acc.w = fmaf(in[t], b.w, acc.w);
-      }
-      *reinterpret_cast<float4*>(out + 4 * q4) = acc;
+      if (rs != nullptr) *reinterpret_cast<float4*>(rs + 4 * q4) = acc.v[q4];
+      gT[static_cast<int64_t>(4 * q4) * d + c] = acc.v[q4].x;
+      gT[static_cast<int64_t>(4 * q4 + 1) * d + c] = acc.v[q4].y;
+      gT[static_cast<int64_t>(4 * q4 + 2) * d + c] = acc.v[q4].z;
+      gT[static_cast<int64_t>(4 * q4 + 3) * d + c] = acc.v[q4].w;
     }
   }
+}
+
+__device__ __forceinline__ float row_get(const RowAcc& acc, int j) {
+  // j is a compile-time index after unrolling
+  const float4 q = acc.v[j >> 2];
+  return (j & 3) == 0 ? q.x : (j & 3) == 1 ? q.y : (j & 3) == 2 ? q.z : q.w;
 }
 
 __device__ __forceinline__ void load_square(float* dst, const float* src, int lp) {
   for (int idx = threadIdx.x * 4; idx < lp * lp; idx += blockDim.x * 4)
     *reinterpret_cast<float4*>(dst + idx) = *reinterpret_cast<const float4*>(src + idx);
+}
+
+__device__ __forceinline__ int64_t rows_at(int i, int d, int lp) {
+  return static_cast<int64_t>(i) * d * lp;
 }
 
 // X (Omega, or Z T with T = R^-1 of the previous orthonormalisation), then
@@ -370,56 +353,50 @@ __global__ void __launch_bounds__(kRowThreads)
   float* Ps = Xs + d * lp;           // [d][lp]
   float* Ts = Ps + d * lp;           // [lp][lp]
   const int c = threadIdx.x;
-  const int64_t rowoff = static_cast<int64_t>(i) * d * lp + static_cast<int64_t>(c) * lp;
+  float* XT = a.X + rows_at(i, d, lp);
   if (kFromZ) {
     load_square(Ts, a.T + static_cast<int64_t>(i) * lp * lp, lp);
     __syncthreads();
     if (c < d) {
-      // this thread's row of Z, staged in its (not yet used) row of Ps
-      float* zr = Ps + c * lp;
-#pragma unroll
-      for (int q4 = 0; q4 < kLmax / 4; ++q4)
-        if (4 * q4 < lp) *reinterpret_cast<float4*>(zr + 4 * q4) =
-            *reinterpret_cast<const float4*>(a.Z + rowoff + 4 * q4);
-      row_times(zr, Ts, Xs + c * lp, l, lp);
+      RowAcc xr;
+      row_zero(xr);
+      row_times(a.Z + rows_at(i, d, lp), d, c, Ts, xr, l, lp);
+      row_store(xr, Xs + c * lp, XT, d, c, lp);
     }
   } else if (c < d) {
-    for (int j = 0; j < lp; ++j) Xs[c * lp + j] = j < l ? __ldg(a.omega + c * l + j) : 0.0f;
-  }
-  if (c < d) {
-#pragma unroll
-    for (int q4 = 0; q4 < kLmax / 4; ++q4)
-      if (4 * q4 < lp) *reinterpret_cast<float4*>(a.X + rowoff + 4 * q4) =
-          *reinterpret_cast<const float4*>(Xs + c * lp + 4 * q4);
+    for (int j = 0; j < lp; ++j) {
+      const float v = j < l ? __ldg(a.omega + c * l + j) : 0.0f;
+      Xs[c * lp + j] = v;
+      XT[static_cast<int64_t>(j) * d + c] = v;
+    }
   }
   __syncthreads();
   if (c < d) {
-    float4 acc[kLmax / 4];
-#pragma unroll
-    for (int q4 = 0; q4 < kLmax / 4; ++q4) acc[q4] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    // P1 row c = sum_k M(c, k) X[k]; M(c, k) is column c of the stored
+    // (transposed) Gram, read 16 rows of k ahead
+    RowAcc acc;
+    row_zero(acc);
     const float* Mc = a.M + static_cast<int64_t>(i) * d * d + c;
-#pragma unroll 4
-    for (int k = 0; k < d; ++k) {
-      const float m = __ldg(Mc + k * d);
-      const float* xr = Xs + k * lp;
+    for (int kb = 0; kb < d; kb += 16) {
+      float mv[16];
 #pragma unroll
-      for (int q4 = 0; q4 < kLmax / 4; ++q4) {
-        if (4 * q4 < lp) {
-          const float4 xv = *reinterpret_cast<const float4*>(xr + 4 * q4);
-          acc[q4].x = fmaf(m, xv.x, acc[q4].x);
-          acc[q4].y = fmaf(m, xv.y, acc[q4].y);
-          acc[q4].z = fmaf(m, xv.z, acc[q4].z);
-          acc[q4].w = fmaf(m, xv.w, acc[q4].w);
+      for (int u = 0; u < 16; ++u) mv[u] = __ldg(Mc + (kb + u) * d);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const float* xr = Xs + (kb + u) * lp;
+#pragma unroll
+        for (int q4 = 0; q4 < kLmax / 4; ++q4) {
+          if (4 * q4 < lp) {
+            const float4 xv = *reinterpret_cast<const float4*>(xr + 4 * q4);
+            acc.v[q4].x = fmaf(mv[u], xv.x, acc.v[q4].x);
+            acc.v[q4].y = fmaf(mv[u], xv.y, acc.v[q4].y);
+            acc.v[q4].z = fmaf(mv[u], xv.z, acc.v[q4].z);
+            acc.v[q4].w = fmaf(mv[u], xv.w, acc.v[q4].w);
+          }
         }
       }
     }
-#pragma unroll
-    for (int q4 = 0; q4 < kLmax / 4; ++q4) {
-      if (4 * q4 < lp) {
-        *reinterpret_cast<float4*>(Ps + c * lp + 4 * q4) = acc[q4];
-        *reinterpret_cast<float4*>(a.P1 + rowoff + 4 * q4) = acc[q4];
-      }
-    }
+    row_store(acc, Ps + c * lp, a.P1 + rows_at(i, d, lp), d, c, lp);
   }
   __syncthreads();
   gram_blocks(Xs, Ps, a.G + static_cast<int64_t>(i) * lp * lp, d, lp);
@@ -435,317 +412,17 @@ __global__ void __launch_bounds__(kRowThreads)
   extern __shared__ float sh[];
   float* Ts = sh;                    // [lp][lp]
   float* Zs = Ts + lp * lp;          // [d][lp]
-  float* Pin = Zs + d * lp;          // [d][lp] rows of P1
   const int c = threadIdx.x;
   load_square(Ts, a.T + static_cast<int64_t>(i) * lp * lp, lp);
   __syncthreads();
   if (c < d) {
-    const int64_t rowoff = static_cast<int64_t>(i) * d * lp + static_cast<int64_t>(c) * lp;
-    float* pr = Pin + c * lp;
-#pragma unroll
-    for (int q4 = 0; q4 < kLmax / 4; ++q4)
-      if (4 * q4 < lp) *reinterpret_cast<float4*>(pr + 4 * q4) =
-          *reinterpret_cast<const float4*>(a.P1 + rowoff + 4 * q4);
-    row_times(pr, Ts, Zs + c * lp, l, lp);
-#pragma unroll
-    for (int q4 = 0; q4 < kLmax / 4; ++q4)
-      if (4 * q4 < lp) *reinterpret_cast<float4*>(a.Z + rowoff + 4 * q4) =
-          *reinterpret_cast<const float4*>(Zs + c * lp + 4 * q4);
+    RowAcc zr;
+    row_zero(zr);
+    row_times(a.P1 + rows_at(i, d, lp), d, c, Ts, zr, l, lp);
+    row_store(zr, Zs + c * lp, a.Z + rows_at(i, d, lp), d, c, lp);
   }
   __syncthreads();
   gram_blocks(Zs, Zs, a.G + static_cast<int64_t>(i) * lp * lp, d, lp);
-}
-
-// ============================================================ l x l, warp
-// Upper-triangular R with G = R^T R (row stride ls): right-looking, one warp,
-// the trailing update uses the unscaled pivot row and rows are scaled at the
-// end.  pik lists the (i, k >= i) pairs row by row, i in the high byte.  A
-// pivot below 1e-6 of its column's squared norm marks a dependent column:
-// keep[j] = 0 and row j zero.
-__device__ void wchol(const float* G, float* R, int* keep, float* dinv, const uint16_t* pik,
-                      int l, int ls, int lane) {
-  const int npairs = l * (l + 1) / 2;
-  for (int idx = lane; idx < l * l; idx += 32) {
-    const int i = idx / l, k = idx - (idx / l) * l;
-    R[i * ls + k] = (k >= i) ? G[i * ls + k] : 0.0f;
-  }
-  __syncwarp();
-  for (int j = 0; j < l; ++j) {
-    const float gjj = G[j * ls + j];
-    const float piv = R[j * ls + j];
-    const bool ok = gjj > 0.0f && piv > 1e-6f * gjj;
-    const float inv2 = ok ? 1.0f / piv : 0.0f;
-    if (lane == 0) {
-      keep[j] = ok ? 1 : 0;
-      dinv[j] = ok ? rsqrtf(piv) : 0.0f;
-    }
-    const int first = (j + 1) * l - ((j + 1) * j) / 2;
-    for (int p = first + lane; p < npairs; p += 32) {
-      const int i = pik[p] >> 8, k = pik[p] & 255;
-      R[i * ls + k] = fmaf(-R[j * ls + i] * inv2, R[j * ls + k], R[i * ls + k]);
-    }
-    __syncwarp();
-  }
-  for (int p = lane; p < npairs; p += 32) {
-    const int i = pik[p] >> 8, k = pik[p] & 255;
-    R[i * ls + k] *= dinv[i];
-  }
-  __syncwarp();
-}
-
-// Ri = R^-1 (stride ls) for upper-triangular R: back substitution from the
-// last row up, rows scaled at the end; dropped indices stay zero.
-__device__ void wtri_inv(const float* R, const int* keep, float* Ri, int l, int ls, int lane) {
-  for (int idx = lane; idx < l * l; idx += 32) {
-    const int i = idx / l, j = idx - (idx / l) * l;
-    Ri[i * ls + j] = (i == j && keep[i]) ? 1.0f : 0.0f;
-  }
-  __syncwarp();
-  for (int i = l - 1; i > 0; --i) {
-    const float inv = keep[i] ? 1.0f / R[i * ls + i] : 0.0f;
-    const int w = l - i;
-    for (int it = lane; it < i * w; it += 32) {
-      const int m = it / w, col = i + (it - (it / w) * w);
-      Ri[m * ls + col] = fmaf(-R[m * ls + i], Ri[i * ls + col] * inv, Ri[m * ls + col]);
-    }
-    __syncwarp();
-  }
-  for (int idx = lane; idx < l * l; idx += 32) {
-    const int i = idx / l, j = idx - (idx / l) * l;
-    Ri[i * ls + j] *= keep[i] ? 1.0f / R[i * ls + i] : 0.0f;
-  }
-  __syncwarp();
-}
-
-// C = op(A) B (l x l, stride ls), op(A) = A or A^T, t ascending.
-__device__ void wmm(const float* A, bool transA, const float* B, float* C, int l, int ls,
-                    int lane) {
-  for (int idx = lane; idx < l * l; idx += 32) {
-    const int i = idx / l, j = idx - (idx / l) * l;
-    float acc = 0.0f;
-    for (int t = 0; t < l; ++t)
-      acc = fmaf(transA ? A[t * ls + i] : A[i * ls + t], B[t * ls + j], acc);
-    C[i * ls + j] = acc;
-  }
-  __syncwarp();
-}
-
-__device__ __forceinline__ void build_pik(uint16_t* pik, int l) {
-  if (threadIdx.x == 0) {
-    int p = 0;
-    for (int i = 0; i < l; ++i)
-      for (int k = i; k < l; ++k) pik[p++] = static_cast<uint16_t>((i << 8) | k);
-  }
-}
-
-// kQr2 = false: T = R^-1 of G.  kQr2 = true: CholeskyQR2 of the implicit
-// iterate whose Gram is G: T = R1^-1 R2^-1 with R2 from Ri1^T G Ri1.
-template <bool kQr2>
-__global__ void __launch_bounds__(kSmallWarps * 32)
-    chol_kernel(const StageArgs a, const __grid_constant__ SegTable seg) {
-  const int l = a.l, lp = a.lp, ls = lp + 1;
-  extern __shared__ float sh[];
-  uint16_t* pik = reinterpret_cast<uint16_t*>(sh);
-  float* base = sh + ((kLmax * (kLmax + 1) / 2) * 2 + 15) / 16 * 4;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* A0 = base + warp * (3 * lp * ls + 2 * kLmax);
-  float* A1 = A0 + lp * ls;
-  float* A2 = A1 + lp * ls;
-  int* keep = reinterpret_cast<int*>(A2 + lp * ls);
-  float* dinv = reinterpret_cast<float*>(keep + kLmax);
-  build_pik(pik, l);
-  __syncthreads();
-  const int i = blockIdx.x * kSmallWarps + warp;
-  if (i >= a.nm) return;
-  const Mat x = decode_mat(a, seg, a.m0 + i);
-  if (x.skip) return;
-  const float* Gg = a.G + static_cast<int64_t>(i) * lp * lp;
-  for (int idx = lane; idx < l * l; idx += 32) {
-    const int r = idx / l, cc = idx - (idx / l) * l;
-    A0[r * ls + cc] = Gg[r * lp + cc];
-  }
-  __syncwarp();
-  const float* out;
-  if (!kQr2) {
-    wchol(A0, A1, keep, dinv, pik, l, ls, lane);            // R in A1
-    wtri_inv(A1, keep, A2, l, ls, lane);                    // Ri in A2
-    out = A2;
-  } else {
-    wchol(A0, A1, keep, dinv, pik, l, ls, lane);            // R1 in A1
-    wtri_inv(A1, keep, A2, l, ls, lane);                    // Ri1 in A2
-    wmm(A0, false, A2, A1, l, ls, lane);                    // H = G Ri1 in A1
-    wmm(A2, true, A1, A0, l, ls, lane);                     // G2 = Ri1^T H in A0
-    wchol(A0, A1, keep, dinv, pik, l, ls, lane);            // R2 in A1
-    // Ri2 into A0 (G2 is no longer needed), then RiY = Ri1 Ri2 into A1
-    wtri_inv(A1, keep, A0, l, ls, lane);
-    wmm(A2, false, A0, A1, l, ls, lane);
-    out = A1;
-  }
-  float* Tg = a.T + static_cast<int64_t>(i) * lp * lp;
-  for (int idx = lane; idx < lp * lp; idx += 32) {
-    const int r = idx / lp, cc = idx - (idx / lp) * lp;
-    Tg[idx] = (r < l && cc < l) ? out[r * ls + cc] : 0.0f;
-  }
-}
-
-// Parallel cyclic Jacobi (round-robin pairing) of the symmetric l x l matrix
-// B B^T = G, one warp per matrix: on return Ub holds the eigenvectors as
-// columns sorted by descending eigenvalue, lam the eigenvalues, and the
-// sigma / eff_rank outputs are written.  Rotation criterion and update
-// formulas are those of the single-kernel builder.
-__global__ void __launch_bounds__(kSmallWarps * 32)
-    jacobi_kernel(const StageArgs a, const __grid_constant__ SegTable seg) {
-  const int l = a.l, lp = a.lp, ls = lp + 1;
-  const int n = (l + 1) & ~1;
-  const int np = n / 2;
-  extern __shared__ float sh[];
-  uint16_t* items = reinterpret_cast<uint16_t*>(sh);        // A blocks then V entries
-  const int n_items = np * np + np * l;
-  float* base = sh + ((kLmax / 2) * (kLmax / 2) + (kLmax / 2) * kLmax + 1) / 2;
-  base = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(base) + 15) & ~uintptr_t(15));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int per_warp = 2 * lp * ls + 4 * kLmax;
-  float* A = base + warp * per_warp;
-  float* V = A + lp * ls;
-  float* cs = V + lp * ls;                                  // 2 per pair
-  int* pairs = reinterpret_cast<int*>(cs + kLmax);          // 2 per pair
-  float* lamv = reinterpret_cast<float*>(pairs + kLmax);    // kLmax
-  int* order = reinterpret_cast<int*>(lamv + kLmax);        // kLmax (overlays nothing else)
-  for (int idx = threadIdx.x; idx < n_items; idx += blockDim.x)
-    items[idx] = idx < np * np ? static_cast<uint16_t>(((idx / np) << 8) | (idx % np))
-                               : static_cast<uint16_t>((((idx - np * np) / l) << 8) |
-                                                       ((idx - np * np) % l));
-  __syncthreads();
-  const int i = blockIdx.x * kSmallWarps + warp;
-  if (i >= a.nm) return;
-  const Mat x = decode_mat(a, seg, a.m0 + i);
-  if (x.skip) return;
-  const float* Gg = a.G + static_cast<int64_t>(i) * lp * lp;
-  for (int idx = lane; idx < l * l; idx += 32) {
-    const int r = idx / l, cc = idx - (idx / l) * l;
-    A[r * ls + cc] = Gg[r * lp + cc];
-    V[r * ls + cc] = (r == cc) ? 1.0f : 0.0f;
-  }
-  __syncwarp();
-  for (int sweep = 0; sweep < kSweeps; ++sweep) {
-    float dmax = 0.0f;
-    for (int r = lane; r < l; r += 32) dmax = fmaxf(dmax, fabsf(A[r * ls + r]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
-    const float abs_tol = 2e-7f * dmax;
-    int active = 0;
-    for (int idx = lane; idx < l * l; idx += 32) {
-      const int p = idx / l, q = idx - (idx / l) * l;
-      if (p < q) {
-        const float apq = A[p * ls + q], app = A[p * ls + p], aqq = A[q * ls + q];
-        if (fabsf(apq) > fmaxf(1e-7f * sqrtf(fabsf(app * aqq)), abs_tol)) active = 1;
-      }
-    }
-    if (!__any_sync(0xffffffffu, active)) break;
-    int rotated = 0;
-    for (int round = 0; round < n - 1; ++round) {
-      if (lane < np) {
-        const int k = lane;
-        int pa, pb;
-        if (k == 0) {
-          pa = n - 1;
-          pb = round;
-        } else {
-          pa = (round + k) % (n - 1);
-          pb = (round - k + (n - 1)) % (n - 1);
-        }
-        if (pa > pb) {
-          const int t = pa;
-          pa = pb;
-          pb = t;
-        }
-        float c = 1.0f, sn = 0.0f;
-        if (pb < l) {
-          const float apq = A[pa * ls + pb];
-          const float app = A[pa * ls + pa], aqq = A[pb * ls + pb];
-          const float tol = fmaxf(1e-7f * sqrtf(fabsf(app * aqq)), abs_tol);
-          if (fabsf(apq) > tol) {
-            const float theta = (aqq - app) / (2.0f * apq);
-            const float tt = copysignf(1.0f, theta) / (fabsf(theta) + sqrtf(theta * theta + 1.0f));
-            c = rsqrtf(tt * tt + 1.0f);
-            sn = tt * c;
-            rotated = 1;
-          }
-        }
-        pairs[2 * k] = pa;
-        pairs[2 * k + 1] = pb;
-        cs[2 * k] = c;
-        cs[2 * k + 1] = sn;
-      }
-      __syncwarp();
-      for (int idx = lane; idx < n_items; idx += 32) {
-        const int it8 = items[idx] >> 8, itl = items[idx] & 255;
-        if (idx < np * np) {
-          const int u = it8, v = itl;
-          const int a0 = pairs[2 * u], b0 = pairs[2 * u + 1];
-          const int a2 = pairs[2 * v], b2 = pairs[2 * v + 1];
-          const float cu = cs[2 * u], su = cs[2 * u + 1];
-          const float cv = cs[2 * v], sv = cs[2 * v + 1];
-          if (su == 0.0f && sv == 0.0f) continue;
-          const bool rb = b0 < l, cb = b2 < l;
-          const float x00 = A[a0 * ls + a2];
-          const float x01 = cb ? A[a0 * ls + b2] : 0.0f;
-          const float x10 = rb ? A[b0 * ls + a2] : 0.0f;
-          const float x11 = (rb && cb) ? A[b0 * ls + b2] : 0.0f;
-          const float y00 = cu * x00 - su * x10, y01 = cu * x01 - su * x11;
-          const float y10 = su * x00 + cu * x10, y11 = su * x01 + cu * x11;
-          A[a0 * ls + a2] = cv * y00 - sv * y01;
-          if (cb) A[a0 * ls + b2] = sv * y00 + cv * y01;
-          if (rb) A[b0 * ls + a2] = cv * y10 - sv * y11;
-          if (rb && cb) A[b0 * ls + b2] = sv * y10 + cv * y11;
-        } else {
-          const int k = it8, r = itl;
-          const int pa = pairs[2 * k], pb = pairs[2 * k + 1];
-          const float sn = cs[2 * k + 1];
-          if (pb >= l || sn == 0.0f) continue;
-          const float c = cs[2 * k];
-          const float vx = V[r * ls + pa], vy = V[r * ls + pb];
-          V[r * ls + pa] = c * vx - sn * vy;
-          V[r * ls + pb] = sn * vx + c * vy;
-        }
-      }
-      __syncwarp();
-    }
-    if (!__any_sync(0xffffffffu, rotated)) break;
-  }
-  // eigenvalues, descending order (ties to the lower index)
-  for (int r = lane; r < l; r += 32) lamv[r] = fmaxf(A[r * ls + r], 0.0f);
-  __syncwarp();
-  for (int r = lane; r < l; r += 32) {
-    int rank = 0;
-    for (int k = 0; k < l; ++k)
-      rank += (lamv[k] > lamv[r] || (lamv[k] == lamv[r] && k < r)) ? 1 : 0;
-    order[rank] = r;
-  }
-  __syncwarp();
-  float* Ubg = a.Ub + static_cast<int64_t>(i) * lp * lp;
-  for (int idx = lane; idx < lp * lp; idx += 32) {
-    const int r = idx / lp, j = idx - (idx / lp) * lp;
-    Ubg[idx] = (r < l && j < l) ? V[r * ls + order[j]] : 0.0f;
-  }
-  float* lg = a.lam + static_cast<int64_t>(i) * lp;
-  for (int j = lane; j < lp; j += 32) lg[j] = j < l ? lamv[order[j]] : 0.0f;
-  if (lane == 0) {
-    const int64_t mi = static_cast<int64_t>(x.unit) * 2 + x.kv;
-    const float total = a.ss[i];
-    float* sg = a.sigma != nullptr ? a.sigma + mi * l : nullptr;
-    float cum = 0.0f;
-    int er = l + 1;
-    const float target = a.energy_frac * total;
-    for (int k = 0; k < l; ++k) {
-      const float lk = lamv[order[k]];
-      if (sg != nullptr) sg[k] = sqrtf(lk);
-      cum += lk;
-      if (er == l + 1 && cum >= target) er = k + 1;
-    }
-    if (!(total > 0.0f)) er = 0;
-    if (a.eff_rank != nullptr) a.eff_rank[mi] = er;
-  }
 }
 
 // W = Z Ub_r diag(1 / sigma_r) (the output factor; directions with sigma at
@@ -760,123 +437,136 @@ __global__ void __launch_bounds__(kRowThreads)
   float* Ts = sh;                    // R_Y^-1 [lp][lp]
   float* Us = Ts + lp * lp;          // Ub [lp][lp]
   float* ls_ = Us + lp * lp;         // lam [lp]
-  float* Rin = ls_ + lp;             // [d][lp] rows of Z, then of X
-  float* Rt = Rin + d * lp;          // [d][lp] rows of X R_Y^-1
+  float* TtT = ls_ + lp;             // (X R_Y^-1) transposed [lp][d]
   load_square(Ts, a.T + static_cast<int64_t>(i) * lp * lp, lp);
   load_square(Us, a.Ub + static_cast<int64_t>(i) * lp * lp, lp);
   for (int j = threadIdx.x; j < lp; j += blockDim.x) ls_[j] = a.lam[static_cast<int64_t>(i) * lp + j];
   __syncthreads();
   const int c = threadIdx.x;
   if (c >= d) return;
-  const int64_t rowoff = static_cast<int64_t>(i) * d * lp + static_cast<int64_t>(c) * lp;
-  float* zr = Rin + c * lp;
-  float* tr = Rt + c * lp;
-#pragma unroll
-  for (int q4 = 0; q4 < kLmax / 4; ++q4)
-    if (4 * q4 < lp) *reinterpret_cast<float4*>(zr + 4 * q4) =
-        *reinterpret_cast<const float4*>(a.Z + rowoff + 4 * q4);
+  RowAcc acc;
+  row_zero(acc);
+  row_times(a.Z + rows_at(i, d, lp), d, c, Us, acc, l, lp);     // (Z Ub) row c
   const float sig_max = sqrtf(ls_[0]);
   __nv_bfloat16* Wo = reinterpret_cast<__nv_bfloat16*>(a.W[x.kv]) +
                       static_cast<int64_t>(x.unit) * d * a.A * r +
                       (static_cast<int64_t>(c) * a.A + x.slot) * r;
-  for (int j = 0; j < r; ++j) {
-    float v = 0.0f;
-    if (j < l) {
-      const float sj = sqrtf(ls_[j]);
-      if (sj > 1e-6f * sig_max && sj > 0.0f) {
-        float acc = 0.0f;
-        for (int t = 0; t < l; ++t) acc = fmaf(zr[t], Us[t * lp + j], acc);
-        v = acc / sj;
-      }
-    }
-    Wo[j] = __float2bfloat16_rn(v);
-  }
-  // tr = X R_Y^-1 (row c), then P = tr Ub_r diag(sigma_r)
 #pragma unroll
-  for (int q4 = 0; q4 < kLmax / 4; ++q4)
-    if (4 * q4 < lp) *reinterpret_cast<float4*>(zr + 4 * q4) =
-        *reinterpret_cast<const float4*>(a.X + rowoff + 4 * q4);
-  row_times(zr, Ts, tr, l, lp);
-  float* Po = a.P + static_cast<int64_t>(i) * d * r + static_cast<int64_t>(c) * r;
-  for (int j = 0; j < r; ++j) {
-    float v = 0.0f;
-    if (j < l) {
-      float acc = 0.0f;
-      for (int t = 0; t < l; ++t) acc = fmaf(tr[t], Us[t * lp + j], acc);
-      v = acc * sqrtf(ls_[j]);
+  for (int j = 0; j < kLmax; ++j) {
+    if (j < r) {
+      float v = 0.0f;
+      if (j < l) {
+        const float sj = sqrtf(ls_[j]);
+        if (sj > 1e-6f * sig_max && sj > 0.0f) v = row_get(acc, j) / sj;
+      }
+      Wo[j] = __float2bfloat16_rn(v);
     }
-    Po[j] = v;
   }
+  // (X R_Y^-1) row c, kept transposed in shared memory, then P = that Ub_r diag(sigma_r)
+  row_zero(acc);
+  row_times(a.X + rows_at(i, d, lp), d, c, Ts, acc, l, lp);
+#pragma unroll
+  for (int j = 0; j < kLmax; ++j)
+    if (j < lp) TtT[j * d + c] = row_get(acc, j);
+  row_zero(acc);
+  row_times(TtT, d, c, Us, acc, l, lp);
+  float* Po = a.P + static_cast<int64_t>(i) * d * r + static_cast<int64_t>(c) * r;
+#pragma unroll
+  for (int j = 0; j < kLmax; ++j)
+    if (j < r) Po[j] = j < l ? row_get(acc, j) * sqrtf(ls_[j]) : 0.0f;
 }
 
-// U = delta P over the segment's rows (zero rows up to Tmax); for pool
+// U = delta P over the segment's rows (zero rows up to Tmax).  The exact and
+// reference rows stream through shared memory in 64-row tiles (cp.async,
+// 16-byte coalesced chunks, two stages, rows past the segment zero-filled);
+// thread = (row of the tile, a quarter of the r columns), delta formed in
+// fp32 from the bf16 pair, features summed in ascending order.  For pool
 // insertion (summaries != nullptr) the K matrix also writes the slot's
 // summary, the mean of the held keys.
+constexpr int kUTile = 64;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n)
+               : "memory");
+}
+
 __global__ void __launch_bounds__(kUThreads)
     u_kernel(const StageArgs a, const __grid_constant__ SegTable seg) {
   const int i = blockIdx.x;
   const Mat x = decode_mat(a, seg, a.m0 + i);
   if (x.skip) return;
   const int d = a.d, r = a.r;
+  const int rowB = d * 2 + 16;                              // padded tile row (bytes)
   extern __shared__ float sh[];
   float* Ps = sh;                                           // [d][r]
+  uint8_t* tiles = reinterpret_cast<uint8_t*>(Ps + d * r);  // [2 stages][exact, ref][kUTile][rowB]
+  const int stageB = 2 * kUTile * rowB;
   const float* Pg = a.P + static_cast<int64_t>(i) * d * r;
   for (int idx = threadIdx.x; idx < d * r; idx += blockDim.x) Ps[idx] = Pg[idx];
-  __syncthreads();
   const __nv_bfloat16* ex = rows_of(a.exact[x.kv], a.es[x.kv], seg, x);
   const __nv_bfloat16* rf = rows_of(a.ref[x.kv], a.rs[x.kv], seg, x);
   const int64_t es3 = a.es[x.kv][3], rs3 = a.rs[x.kv][3];
+  const int chunks = d / 8;                                 // 16-byte chunks per row
+  const int ntiles = (a.Tmax + kUTile - 1) / kUTile;
+  auto issue = [&](int tile, int stage) {
+    uint8_t* te = tiles + stage * stageB;
+    uint8_t* tr = te + kUTile * rowB;
+    for (int q = threadIdx.x; q < kUTile * chunks; q += blockDim.x) {
+      const int row = q / chunks, ch = q - (q / chunks) * chunks;
+      const int t = tile * kUTile + row;
+      const bool in = t < x.n;
+      const int ts = in ? t : 0;
+      cp_async16(te + row * rowB + ch * 16, ex + ts * es3 + ch * 8, in);
+      cp_async16(tr + row * rowB + ch * 16, rf + ts * rs3 + ch * 8, in);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  issue(0, 0);
+  const int row = threadIdx.x >> 2;                         // 0..63
+  const int jw = r >> 2;                                    // columns per thread (r % 8 == 0)
+  const int j0 = (threadIdx.x & 3) * jw;
   __nv_bfloat16* Uo = reinterpret_cast<__nv_bfloat16*>(a.U[x.kv]) +
                       static_cast<int64_t>(x.unit) * a.Tmax * a.A * r;
-  constexpr int VEC = 8;                                    // bf16 per 16-byte load
-  const bool vec_r = (r & 3) == 0;
-  for (int t = threadIdx.x; t < a.Tmax; t += blockDim.x) {
-    __nv_bfloat16* urow = Uo + (static_cast<int64_t>(t) * a.A + x.slot) * r;
-    for (int j0 = 0; j0 < r; j0 += 32) {
-      float4 acc[8];
+  for (int tile = 0; tile < ntiles; ++tile) {
+    const int stage = tile & 1;
+    if (tile + 1 < ntiles) {
+      issue(tile + 1, stage ^ 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();
+    const uint8_t* te = tiles + stage * stageB + row * rowB;
+    const uint8_t* tr = te + kUTile * rowB;
+    float acc[kLmax / 4];
 #pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) acc[q4] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      if (t < x.n) {
-        for (int c0 = 0; c0 < d; c0 += VEC) {
-          const uint4 xe = *reinterpret_cast<const uint4*>(ex + t * es3 + c0);
-          const uint4 xr = *reinterpret_cast<const uint4*>(rf + t * rs3 + c0);
-          const __nv_bfloat16* pe = reinterpret_cast<const __nv_bfloat16*>(&xe);
-          const __nv_bfloat16* pq = reinterpret_cast<const __nv_bfloat16*>(&xr);
+    for (int jj = 0; jj < kLmax / 4; ++jj) acc[jj] = 0.0f;
+#pragma unroll 2
+    for (int c = 0; c < d; c += 2) {
+      const float2 e2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(te + c * 2));
+      const float2 r2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(tr + c * 2));
+      const float d0 = e2.x - r2.x, d1 = e2.y - r2.y;
+      const float* p0 = Ps + c * r + j0;
+      const float* p1 = p0 + r;
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const float dv = __bfloat162float(pe[e]) - __bfloat162float(pq[e]);
-            const float* pr = Ps + (c0 + e) * r + j0;
-            if (vec_r) {
-#pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4) {
-                if (j0 + 4 * q4 < r) {
-                  const float4 pv = *reinterpret_cast<const float4*>(pr + 4 * q4);
-                  acc[q4].x = fmaf(dv, pv.x, acc[q4].x);
-                  acc[q4].y = fmaf(dv, pv.y, acc[q4].y);
-                  acc[q4].z = fmaf(dv, pv.z, acc[q4].z);
-                  acc[q4].w = fmaf(dv, pv.w, acc[q4].w);
-                }
-              }
-            } else {
-#pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4) {
-                float* av = reinterpret_cast<float*>(&acc[q4]);
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                  if (j0 + 4 * q4 + u < r) av[u] = fmaf(dv, pr[4 * q4 + u], av[u]);
-              }
-            }
-          }
+      for (int jj = 0; jj < kLmax / 4; ++jj) {
+        if (jj < jw) {
+          acc[jj] = fmaf(d0, p0[jj], acc[jj]);
+          acc[jj] = fmaf(d1, p1[jj], acc[jj]);
         }
       }
-#pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) {
-        const float* av = reinterpret_cast<const float*>(&acc[q4]);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (j0 + 4 * q4 + u < r) urow[j0 + 4 * q4 + u] = __float2bfloat16_rn(av[u]);
-      }
     }
+    const int t = tile * kUTile + row;
+    if (t < a.Tmax) {
+      __nv_bfloat16* urow = Uo + (static_cast<int64_t>(t) * a.A + x.slot) * r + j0;
+#pragma unroll
+      for (int jj = 0; jj < kLmax / 4; jj += 2)
+        if (jj < jw)
+          *reinterpret_cast<__nv_bfloat162*>(urow + jj) = __floats2bfloat162_rn(acc[jj], acc[jj + 1]);
+    }
+    __syncthreads();                                        // the stage is refilled two tiles on
   }
   if (a.summaries != nullptr && x.kv == 0) {
     float* smy = a.summaries + (static_cast<int64_t>(x.unit) * a.A + x.slot) * d;
@@ -926,6 +616,58 @@ template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(bytes));
+}
+
+// Every stage over the matrices of each pass.
+cudaError_t run_passes(StageArgs& a, const SegTable& seg, int64_t mats, int64_t NM, int q,
+                       const DeviceInfo& di, cudaStream_t stream) {
+  const int d = a.d, lp = a.lp, r = a.r, l = a.l;
+  const size_t gram_smem = 1024 + 2 * 2 * kDP * 128 + 64 + 64;
+  const size_t mx_smem = static_cast<size_t>(2 * d * lp + lp * lp) * sizeof(float);
+  const size_t zg_smem = static_cast<size_t>(lp * lp + d * lp) * sizeof(float);
+  const size_t wp_smem = static_cast<size_t>(2 * lp * lp + lp + lp * d) * sizeof(float);
+  const size_t u_smem = static_cast<size_t>(d * r) * sizeof(float) +
+                        static_cast<size_t>(2 * 2 * kUTile) * (d * 2 + 16);
+  const size_t chol_smem = chol_smem_bytes(false, l);
+  const size_t qr2_smem = chol_smem_bytes(true, l);
+  const size_t eig_smem = eig_smem_bytes(l);
+  cudaError_t e;
+  if ((e = set_smem(gram_kernel, gram_smem)) != cudaSuccess) return e;
+  if ((e = set_smem(mx_kernel<false>, mx_smem)) != cudaSuccess) return e;
+  if ((e = set_smem(mx_kernel<true>, mx_smem)) != cudaSuccess) return e;
+  if ((e = set_smem(zg_kernel, zg_smem)) != cudaSuccess) return e;
+  if ((e = set_smem(wp_kernel, wp_smem)) != cudaSuccess) return e;
+  if ((e = set_smem(u_kernel, u_smem)) != cudaSuccess) return e;
+  // three Gram CTAs fit an SM (64 KB of operand buffers, 128 TMEM columns each)
+  const int gram_slots = di.sm_count * 3;
+  for (int64_t m0 = 0; m0 < mats; m0 += NM) {
+    const int nm = static_cast<int>(std::min<int64_t>(NM, mats - m0));
+    a.m0 = static_cast<int32_t>(m0);
+    a.nm = nm;
+    const int sg = (nm + kSmallWarps - 1) / kSmallWarps;
+    gram_kernel<<<std::min(nm, gram_slots), kGramThreads, gram_smem, stream>>>(a, seg);
+    for (int it = 0; it < q; ++it) {
+      if (it == 0)
+        mx_kernel<false><<<nm, kRowThreads, mx_smem, stream>>>(a, seg);
+      else
+        mx_kernel<true><<<nm, kRowThreads, mx_smem, stream>>>(a, seg);
+      if ((e = launch_chol(a, seg, false, sg, chol_smem, stream)) != cudaSuccess) return e;  // R_Y^-1
+      zg_kernel<<<nm, kRowThreads, zg_smem, stream>>>(a, seg);                             // delta^T Q
+      if ((e = launch_chol(a, seg, false, sg, chol_smem, stream)) != cudaSuccess) return e;  // orth
+    }
+    if (q == 0)
+      mx_kernel<false><<<nm, kRowThreads, mx_smem, stream>>>(a, seg);
+    else
+      mx_kernel<true><<<nm, kRowThreads, mx_smem, stream>>>(a, seg);
+    if ((e = launch_chol(a, seg, true, sg, qr2_smem, stream)) != cudaSuccess) return e;     // QR2
+    zg_kernel<<<nm, kRowThreads, zg_smem, stream>>>(a, seg);                               // B^T, B B^T
+    if ((e = launch_eig(a, seg, sg, eig_smem, stream)) != cudaSuccess) return e;
+    wp_kernel<<<nm, kRowThreads, wp_smem, stream>>>(a, seg);
+    u_kernel<<<nm, kUThreads, u_smem, stream>>>(a, seg);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -1003,59 +745,7 @@ cudaError_t launch_build_staged(const Dims& dm, const SegTable& seg, const View 
   a.lam = reinterpret_cast<float*>(ws + w.lam);
   a.P = reinterpret_cast<float*>(ws + w.P);
 
-  const int ls = lp + 1;
-  const size_t gram_smem = 1024 + 2 * 2 * kDP * 128 + 64 + 64;
-  const size_t mx_smem = static_cast<size_t>(2 * d * lp + lp * lp) * sizeof(float);
-  const size_t zg_smem = static_cast<size_t>(lp * lp + 2 * d * lp) * sizeof(float);
-  const size_t wp_smem = static_cast<size_t>(2 * lp * lp + lp + 2 * d * lp) * sizeof(float);
-  const size_t u_smem = static_cast<size_t>(d * r) * sizeof(float);
-  const size_t pik_bytes = ((kLmax * (kLmax + 1) / 2) * 2 + 15) / 16 * 16;
-  const size_t chol_smem =
-      pik_bytes + static_cast<size_t>(kSmallWarps) * (3 * lp * ls + 2 * kLmax) * sizeof(float);
-  const size_t items_bytes =
-      ((kLmax / 2) * (kLmax / 2) + (kLmax / 2) * kLmax + 1) / 2 * sizeof(float) + 16;
-  const size_t jac_smem =
-      items_bytes + static_cast<size_t>(kSmallWarps) * (2 * lp * ls + 4 * kLmax) * sizeof(float);
-  if ((e = set_smem(gram_kernel, gram_smem)) != cudaSuccess) return e;
-  if ((e = set_smem(mx_kernel<false>, mx_smem)) != cudaSuccess) return e;
-  if ((e = set_smem(mx_kernel<true>, mx_smem)) != cudaSuccess) return e;
-  if ((e = set_smem(zg_kernel, zg_smem)) != cudaSuccess) return e;
-  if ((e = set_smem(wp_kernel, wp_smem)) != cudaSuccess) return e;
-  if ((e = set_smem(u_kernel, u_smem)) != cudaSuccess) return e;
-  if ((e = set_smem(chol_kernel<false>, chol_smem)) != cudaSuccess) return e;
-  if ((e = set_smem(chol_kernel<true>, chol_smem)) != cudaSuccess) return e;
-  if ((e = set_smem(jacobi_kernel, jac_smem)) != cudaSuccess) return e;
-  // three Gram CTAs fit an SM (64 KB of operand buffers, 128 TMEM columns each)
-  const int gram_slots = di.sm_count * 3;
-
-  for (int64_t m0 = 0; m0 < mats; m0 += NM) {
-    const int nm = static_cast<int>(std::min<int64_t>(NM, mats - m0));
-    a.m0 = static_cast<int32_t>(m0);
-    a.nm = nm;
-    const int small_grid = (nm + kSmallWarps - 1) / kSmallWarps;
-    gram_kernel<<<std::min(nm, gram_slots), kGramThreads, gram_smem, stream>>>(a, seg);
-    for (int it = 0; it < q; ++it) {
-      if (it == 0)
-        mx_kernel<false><<<nm, kRowThreads, mx_smem, stream>>>(a, seg);
-      else
-        mx_kernel<true><<<nm, kRowThreads, mx_smem, stream>>>(a, seg);
-      chol_kernel<false><<<small_grid, kSmallWarps * 32, chol_smem, stream>>>(a, seg);   // R_Y^-1
-      zg_kernel<<<nm, kRowThreads, zg_smem, stream>>>(a, seg);                           // delta^T Q
-      chol_kernel<false><<<small_grid, kSmallWarps * 32, chol_smem, stream>>>(a, seg);   // orth
-    }
-    if (q == 0)
-      mx_kernel<false><<<nm, kRowThreads, mx_smem, stream>>>(a, seg);
-    else
-      mx_kernel<true><<<nm, kRowThreads, mx_smem, stream>>>(a, seg);
-    chol_kernel<true><<<small_grid, kSmallWarps * 32, chol_smem, stream>>>(a, seg);      // R_Y^-1 (QR2)
-    zg_kernel<<<nm, kRowThreads, zg_smem, stream>>>(a, seg);                             // B^T, B B^T
-    jacobi_kernel<<<small_grid, kSmallWarps * 32, jac_smem, stream>>>(a, seg);
-    wp_kernel<<<nm, kRowThreads, wp_smem, stream>>>(a, seg);
-    u_kernel<<<nm, kUThreads, u_smem, stream>>>(a, seg);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  return run_passes(a, seg, mats, NM, q, di, stream);
 }
 
 }  // namespace kvc

@@ -344,13 +344,14 @@ def _match_bytes(wl) -> int:
             + wl.S * wl.L * wl.H * wl.A * (wl.d + 1) * 4)
 
 
-def _builder_leg(args, dev, wl_name: str = "longctx"):
+def _builder_leg(args, dev, wl=None):
     """kvc_build_states alone on one edge of a state-building workload (the
     long-context shapes by default: 64 segments x 512 tokens x 32 layers x 8
     heads, K and V = 32,768 matrices of 512 x 128, r = 32, p = 8, q = 2)."""
     import torch
     from agent_shared_context_gb300 import kvc, synth
-    wl = synth.workload(wl_name)
+    if wl is None:
+        wl = synth.workload("longctx")
     inp = synth.generate(wl, device=dev, edges=[1], context_free=False)
     e = inp.edges[0]
     seg = kvc.Segments.from_workload(wl)
@@ -518,11 +519,11 @@ def run_kvc(args, wl):
     # ---- the state builder (its own workload, after the main one is freed)
     builder = None
     if world == 1 and not args.no_builder_leg:
-        build_name = wl.name if runner.build else "longctx"
+        build_wl = wl if runner.build else None
         del runner, inp, e, eo, part, ksum
         gc.collect()
         torch.cuda.empty_cache()
-        builder = _builder_leg(args, dev, build_name)
+        builder = _builder_leg(args, dev, build_wl)
 
     line = {
         "metric": "corrected KV tokens/s (all layers, K+V)",
