@@ -53,19 +53,23 @@ __device__ __forceinline__ WarpMats warp_mats(float* sh, int warp, int l, int nm
   return w;
 }
 
-// Cholesky G = R^T R (G symmetric, column-major, stride cs; R written
-// column-major into R, upper triangle): right-looking with the unscaled pivot
-// row, R[i][k] -= R[j][i] R[j][k] / pivot_j, rows scaled by dinv at the end;
-// a pivot below 1e-6 of its column's squared norm marks a dependent column
-// (keep[j] = 0, row j zero).  diag gets the final R[i][i].
-__device__ void chol_cols(const float* __restrict__ G, float* __restrict__ R, int* keep,
-                          float* dinv, float* diag, int l, int cs, int lane) {
-  for (int k = lane; k < l; k += 32)
-    for (int m = 0; m < l; ++m) R[k * cs + m] = m <= k ? G[k * cs + m] : 0.0f;
+// In-place Cholesky G = R^T R (G symmetric, column-major, stride cs; R
+// overwrites it, upper triangle, zeros below): right-looking with the
+// unscaled pivot row, R[i][k] -= R[j][i] R[j][k] / pivot_j, rows scaled by
+// dinv at the end; a pivot at or below 1e-6 of its column's original squared
+// norm marks a dependent column (keep[j] = 0, row j zero).  Step j writes
+// rows below j only, so every lane may read row j of the other columns while
+// the step runs.  gd is scratch for G's diagonal; diag gets the final R[i][i].
+__device__ void chol_inplace(float* __restrict__ A, int* keep, float* dinv, float* diag,
+                             float* gd, int l, int cs, int lane) {
+  for (int k = lane; k < l; k += 32) {
+    gd[k] = A[k * cs + k];
+    for (int m = k + 1; m < l; ++m) A[k * cs + m] = 0.0f;
+  }
   __syncwarp();
   for (int j = 0; j < l; ++j) {
-    const float gjj = G[j * cs + j];
-    const float piv = R[j * cs + j];
+    const float gjj = gd[j];
+    const float piv = A[j * cs + j];
     const bool ok = gjj > 0.0f && piv > 1e-6f * gjj;
     const float inv2 = ok ? 1.0f / piv : 0.0f;
     if (lane == 0) {
@@ -74,48 +78,46 @@ __device__ void chol_cols(const float* __restrict__ G, float* __restrict__ R, in
     }
     for (int k = lane; k < l; k += 32) {
       if (k <= j) continue;
-      float* rk = R + k * cs;
+      float* rk = A + k * cs;
       const float rjk = rk[j];
       int i = j + 1;
-      // eight rows at a time: every load issued before the stores (the row-j
-      // entries of other columns are not written in this step)
+      // eight rows at a time: every load issued before the stores
       for (; i + 8 <= k + 1; i += 8) {
         float t[8], v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          t[u] = R[(i + u) * cs + j];
+          t[u] = A[(i + u) * cs + j];
           v[u] = rk[i + u];
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) rk[i + u] = fmaf(-t[u] * inv2, rjk, v[u]);
       }
-      for (; i <= k; ++i) rk[i] = fmaf(-R[i * cs + j] * inv2, rjk, rk[i]);
+      for (; i <= k; ++i) rk[i] = fmaf(-A[i * cs + j] * inv2, rjk, rk[i]);
     }
     __syncwarp();
   }
   for (int k = lane; k < l; k += 32) {
-    float* rk = R + k * cs;
+    float* rk = A + k * cs;
     for (int m = 0; m <= k; ++m) rk[m] *= dinv[m];
     diag[k] = rk[k];
   }
   __syncwarp();
 }
 
-// Ri = R^-1 (column-major, upper triangle, stride cs) of the upper-
-// triangular R of chol_cols: back substitution from the last row up,
-// Ri[m][k] -= R[m][i] Ri[i][k] / R[i][i] for m < i <= k, rows scaled at the
-// end; dropped indices stay zero.  Entries below the diagonal are zero.
-__device__ void tri_inv_cols(const float* __restrict__ R, const int* keep, const float* diag,
-                             float* __restrict__ Ri, int l, int cs, int lane) {
-  for (int k = lane; k < l; k += 32)
-    for (int m = 0; m < l; ++m) Ri[k * cs + m] = (m == k && keep[m]) ? 1.0f : 0.0f;
-  __syncwarp();
-  for (int i = l - 1; i > 0; --i) {
+// In-place R^-1 of the upper-triangular R of chol_inplace (column-major,
+// stride cs): back substitution from the last row up.  At step i the lanes
+// owning columns k > i update them, Ri[m][k] -= R[m][i] Ri[i][k] / R[i][i]
+// for m < i, reading column i, which still holds R; after a warp barrier
+// the lanes turn column i into column i of the inverse (element m on lane m).  Rows are scaled
+// by 1 / R[m][m] at the end; dropped indices give zero rows and columns.
+__device__ void tri_inv_inplace(float* __restrict__ A, const int* keep, const float* diag, int l,
+                                int cs, int lane) {
+  for (int i = l - 1; i >= 0; --i) {
     const float inv = keep[i] ? 1.0f / diag[i] : 0.0f;
-    const float* ri = R + i * cs;
+    const float* ri = A + i * cs;
     for (int k = lane; k < l; k += 32) {
-      if (k < i) continue;
-      float* ck = Ri + k * cs;
+      if (k <= i) continue;
+      float* ck = A + k * cs;
       const float xi = ck[i] * inv;
       int m = 0;
       for (; m + 8 <= i; m += 8) {
@@ -131,9 +133,13 @@ __device__ void tri_inv_cols(const float* __restrict__ R, const int* keep, const
       for (; m < i; ++m) ck[m] = fmaf(-ri[m], xi, ck[m]);
     }
     __syncwarp();
+    float* ci = A + i * cs;                                 // element m on lane m
+    for (int m = lane; m < i; m += 32) ci[m] = -ci[m] * inv;
+    if (lane == 0) ci[i] = keep[i] ? 1.0f : 0.0f;
+    __syncwarp();
   }
   for (int k = lane; k < l; k += 32)
-    for (int m = 0; m < l; ++m) Ri[k * cs + m] *= keep[m] ? 1.0f / diag[m] : 0.0f;
+    for (int m = 0; m <= k; ++m) A[k * cs + m] *= keep[m] ? 1.0f / diag[m] : 0.0f;
   __syncwarp();
 }
 
@@ -161,10 +167,23 @@ __device__ void cmm(const float* __restrict__ A, bool transA, const float* __res
 
 __device__ __forceinline__ void load_gram(const float* Gg, float* G, int l, int lp, int cs,
                                           int lane) {
-  // G is symmetric: row r of the global matrix is column r
-  for (int idx = lane; idx < l * l; idx += 32) {
-    const int r = idx / l, c = idx - (idx / l) * l;
-    G[r * cs + c] = Gg[r * lp + c];
+  // G is symmetric: row r of the global matrix is column r.  Eight loads in
+  // flight per lane before the shared-memory stores.
+  const int n = l * l;
+  for (int b = lane; b < n; b += 8 * 32) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int idx = b + 32 * u;
+      const int r = idx / l, c = idx - (idx / l) * l;
+      v[u] = idx < n ? __ldg(Gg + r * lp + c) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int idx = b + 32 * u;
+      const int r = idx / l, c = idx - (idx / l) * l;
+      if (idx < n) G[r * cs + c] = v[u];
+    }
   }
   __syncwarp();
 }
@@ -184,25 +203,30 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
   const int l = a.l, lp = a.lp, cs = col_stride(l);
   extern __shared__ float sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const WarpMats w = warp_mats(sh, warp, l, kQr2 ? 3 : 2);
+  const WarpMats w = warp_mats(sh, warp, l, kQr2 ? 3 : 1);
   const int i = blockIdx.x * kSmallWarps + warp;
   if (i >= a.nm) return;
   const Mat x = decode_mat(a, seg, a.m0 + i);
   if (x.skip) return;
-  load_gram(a.G + static_cast<int64_t>(i) * lp * lp, w.A, l, lp, cs, lane);
-  chol_cols(w.A, w.B, w.keep, w.dinv, w.diag, l, cs, lane);       // R in B
-  float* ri1 = kQr2 ? w.C : w.A;                                  // G is needed again for QR2
-  tri_inv_cols(w.B, w.keep, w.diag, ri1, l, cs, lane);
-  const float* out = ri1;
-  if (kQr2) {
-    cmm(w.A, false, w.C, w.B, l, cs, lane);                       // H = G Ri1      (B)
-    cmm(w.C, true, w.B, w.A, l, cs, lane);                        // G2 = Ri1^T H   (A)
-    chol_cols(w.A, w.B, w.keep, w.dinv, w.diag, l, cs, lane);     // R2             (B)
-    float* ri2 = w.A;                                             // G2 no longer needed
-    tri_inv_cols(w.B, w.keep, w.diag, ri2, l, cs, lane);          // Ri2            (A)
-    cmm(w.C, false, ri2, w.B, l, cs, lane);                       // R_Y^-1 = Ri1 Ri2 (B)
-    out = w.B;
+  if (!kQr2) {
+    load_gram(a.G + static_cast<int64_t>(i) * lp * lp, w.A, l, lp, cs, lane);
+    chol_inplace(w.A, w.keep, w.dinv, w.diag, w.lam, l, cs, lane);   // R      (A)
+    tri_inv_inplace(w.A, w.keep, w.diag, l, cs, lane);               // R^-1   (A)
+    store_cols(w.A, a.T + static_cast<int64_t>(i) * lp * lp, l, lp, cs, lane);
+    return;
   }
+  load_gram(a.G + static_cast<int64_t>(i) * lp * lp, w.A, l, lp, cs, lane);
+  for (int k = lane; k < l; k += 32)                                // G kept in A
+    for (int m = 0; m < l; ++m) w.B[k * cs + m] = w.A[k * cs + m];
+  __syncwarp();
+  chol_inplace(w.B, w.keep, w.dinv, w.diag, w.lam, l, cs, lane);     // R1             (B)
+  tri_inv_inplace(w.B, w.keep, w.diag, l, cs, lane);                 // Ri1            (B)
+  cmm(w.A, false, w.B, w.C, l, cs, lane);                            // H = G Ri1      (C)
+  cmm(w.B, true, w.C, w.A, l, cs, lane);                             // G2 = Ri1^T H   (A)
+  chol_inplace(w.A, w.keep, w.dinv, w.diag, w.lam, l, cs, lane);     // R2             (A)
+  tri_inv_inplace(w.A, w.keep, w.diag, l, cs, lane);                 // Ri2            (A)
+  cmm(w.B, false, w.A, w.C, l, cs, lane);                            // R_Y^-1 = Ri1 Ri2 (C)
+  const float* out = w.C;
   store_cols(out, a.T + static_cast<int64_t>(i) * lp * lp, l, lp, cs, lane);
 }
 
@@ -214,7 +238,9 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
 // accumulator.  Column p of X (row p of R) is read with stride cs from the
 // column-major R.  Round-robin pairing, one pair per lane; a pair is rotated
 // while |y_p . y_q| > max(1e-7 |y_p| |y_q|, 2e-7 max_i |y_i|^2), and the
-// sweeps stop after one that rotates nothing.  Writes Ub (columns sorted by
+// sweeps stop after one that rotates nothing.  The squared column norms are
+// recomputed at the start of each sweep and updated by every rotation, so a
+// round computes one dot product per pair.  Writes Ub (columns sorted by
 // descending eigenvalue), lam and the sigma / eff_rank outputs.
 __global__ void __launch_bounds__(kSmallWarps * 32)
     eig_kernel(const StageArgs a, const __grid_constant__ SegTable seg) {
@@ -223,21 +249,24 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
   const int np = n / 2;
   extern __shared__ float sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const WarpMats w = warp_mats(sh, warp, l, 2);
+  const WarpMats w = warp_mats(sh, warp, l, 1);
   const int i = blockIdx.x * kSmallWarps + warp;
   if (i >= a.nm) return;
   const Mat x = decode_mat(a, seg, a.m0 + i);
   if (x.skip) return;
   load_gram(a.G + static_cast<int64_t>(i) * lp * lp, w.A, l, lp, cs, lane);
-  chol_cols(w.A, w.B, w.keep, w.dinv, w.diag, l, cs, lane);
-  float* Y = w.B;                 // y_p[e] = R[p][e] = Y[e * cs + p]
+  chol_inplace(w.A, w.keep, w.dinv, w.diag, w.lam, l, cs, lane);
+  float* Y = w.A;                 // y_p[e] = R[p][e] = Y[e * cs + p]
+  float* nrm = w.diag;            // |y_p|^2: exact at each sweep's start, then tracked
   for (int sweep = 0; sweep < kSweepsOneSided; ++sweep) {
     float nmax = 0.0f;
     for (int p = lane; p < l; p += 32) {
       float s2 = 0.0f;
       for (int e = 0; e < l; ++e) s2 = fmaf(Y[e * cs + p], Y[e * cs + p], s2);
+      nrm[p] = s2;
       nmax = fmaxf(nmax, s2);
     }
+    __syncwarp();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) nmax = fmaxf(nmax, __shfl_xor_sync(0xffffffffu, nmax, o));
     const float abs_tol = 2e-7f * nmax;
@@ -259,14 +288,10 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
           pb = t;
         }
         if (pb < l) {
-          float app = 0.0f, aqq = 0.0f, apq = 0.0f;
-#pragma unroll 4
-          for (int e = 0; e < l; ++e) {
-            const float u = Y[e * cs + pa], v = Y[e * cs + pb];
-            app = fmaf(u, u, app);
-            aqq = fmaf(v, v, aqq);
-            apq = fmaf(u, v, apq);
-          }
+          const float app = nrm[pa], aqq = nrm[pb];
+          float apq = 0.0f;
+#pragma unroll 8
+          for (int e = 0; e < l; ++e) apq = fmaf(Y[e * cs + pa], Y[e * cs + pb], apq);
           const float tol = fmaxf(1e-7f * sqrtf(app * aqq), abs_tol);
           if (fabsf(apq) > tol) {
             const float theta = (aqq - app) / (2.0f * apq);
@@ -292,6 +317,10 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
               Y[e * cs + pa] = c * u - sn * v;
               Y[e * cs + pb] = sn * u + c * v;
             }
+            // the rotation that zeroes y_p . y_q moves t (y_p . y_q) of
+            // squared norm from column p to column q
+            nrm[pa] = fmaf(-tt, apq, app);
+            nrm[pb] = fmaf(tt, apq, aqq);
             rotated = 1;
           }
         }
@@ -352,8 +381,8 @@ size_t smem_bytes(int l, int nmats) {
 
 }  // namespace
 
-size_t chol_smem_bytes(bool qr2, int l) { return smem_bytes(l, qr2 ? 3 : 2); }
-size_t eig_smem_bytes(int l) { return smem_bytes(l, 2); }
+size_t chol_smem_bytes(bool qr2, int l) { return smem_bytes(l, qr2 ? 3 : 1); }
+size_t eig_smem_bytes(int l) { return smem_bytes(l, 1); }
 
 cudaError_t launch_chol(const StageArgs& a, const SegTable& seg, bool qr2, int grid, size_t smem,
                         cudaStream_t stream) {

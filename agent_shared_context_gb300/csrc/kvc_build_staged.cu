@@ -28,18 +28,20 @@
 //                  sorted, with sigma and the effective rank;
 //   wp_kernel      (thread = feature row) W = Z Ub_r Sigma_r^-1 (output) and
 //                  P = X R_Y^-1 Ub_r Sigma_r (workspace);
-//   u_kernel       U = delta P from 64-row tiles of the exact and reference
-//                  rows (cp.async, two stages), rows past the segment
-//                  zeroed; for pool insertion the held-key mean.
+//   u_kernel       U = delta P on tcgen05 (128-token tiles of delta and P
+//                  split into bf16 hi + lo, three MMAs per 16-feature step,
+//                  two TMEM accumulators), rows past the segment zero; for
+//                  pool insertion the held-key mean.
 //
-// The Gram, the products and the Cholesky / triangular-inverse steps match
-// the single-kernel builder element for element (summation orders included);
-// the final l x l eigenproblem uses one-sided Jacobi on the Cholesky factor
-// (same eigenpairs up to rounding and signs, which U W^T does not see).  The
-// small l x l steps run one matrix per warp -- columns in registers,
-// warp-level synchronisation only -- so a CTA of four warps keeps four of
-// them in flight.  The only wait is the Gram kernel's MMA completion, bounded
-// by kWaitLimitNs.
+// The Gram and the l x l Cholesky / triangular-inverse steps follow the
+// single-kernel builder's arithmetic; the final l x l eigenproblem uses
+// one-sided Jacobi on the Cholesky factor (same eigenpairs up to rounding and
+// signs, which U W^T does not see), and U = delta P runs on the tensor cores
+// with split operands (~2^-16 relative, far below the bf16 rounding of U).
+// The small l x l steps run one matrix per warp in shared memory, factored
+// and inverted in place, with warp-level synchronisation only.  The only
+// waits are the MMA completions of the Gram and U kernels, bounded by
+// kWaitLimitNs.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -274,11 +276,33 @@ __device__ __forceinline__ void gram_blocks(const float* As, const float* Bs, fl
   }
 }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Copy n floats (a multiple of 4, 16-byte aligned) global -> shared with the
+// CTA's threads, 16-byte cp.async chunks; the caller commits.
+__device__ __forceinline__ void stage_floats(float* dst, const float* src, int n) {
+  for (int q = threadIdx.x; q < n / 4; q += blockDim.x) cp_async16(dst + 4 * q, src + 4 * q, true);
+}
+
 // The d x l iterates live in the workspace transposed ([lp][d], entry (c, j)
-// at j * d + c), so the threads of a CTA (thread = feature row c) read and
-// write them coalesced.  A row times an lp x lp matrix runs over t at run
-// time with the lp accumulators in registers (static indices) and the matrix
-// read from shared memory as broadcasts.
+// at j * d + c) and are staged whole into shared memory with cp.async, so
+// the threads of a CTA (thread = feature row c) read them without bank
+// conflicts.  A row times an lp x lp matrix runs over t at run time with the
+// lp accumulators in registers (static indices) and the matrix read from
+// shared memory as broadcasts.
 struct RowAcc {
   float4 v[kLmax / 4];
 };
@@ -293,7 +317,7 @@ __device__ __forceinline__ void row_times(const float* inT, int d, int c, const 
                                           RowAcc& acc, int l, int lp) {
 #pragma unroll 4
   for (int t = 0; t < l; ++t) {
-    const float v = inT[static_cast<int64_t>(t) * d + c];
+    const float v = inT[t * d + c];
     const float* tr = Ts + t * lp;
 #pragma unroll
     for (int q4 = 0; q4 < kLmax / 4; ++q4) {
@@ -330,17 +354,14 @@ __device__ __forceinline__ float row_get(const RowAcc& acc, int j) {
   return (j & 3) == 0 ? q.x : (j & 3) == 1 ? q.y : (j & 3) == 2 ? q.z : q.w;
 }
 
-__device__ __forceinline__ void load_square(float* dst, const float* src, int lp) {
-  for (int idx = threadIdx.x * 4; idx < lp * lp; idx += blockDim.x * 4)
-    *reinterpret_cast<float4*>(dst + idx) = *reinterpret_cast<const float4*>(src + idx);
-}
-
 __device__ __forceinline__ int64_t rows_at(int i, int d, int lp) {
   return static_cast<int64_t>(i) * d * lp;
 }
 
+constexpr int kMRows = 16;       // rows of M per cp.async stage of the M X product
+
 // X (Omega, or Z T with T = R^-1 of the previous orthonormalisation), then
-// P1 = M X and G = X^T P1.
+// P1 = M X and G = X^T P1.  M streams through two 16-row stages.
 template <bool kFromZ>
 __global__ void __launch_bounds__(kRowThreads)
     mx_kernel(const StageArgs a, const __grid_constant__ SegTable seg) {
@@ -350,17 +371,26 @@ __global__ void __launch_bounds__(kRowThreads)
   const int d = a.d, l = a.l, lp = a.lp;
   extern __shared__ float sh[];
   float* Xs = sh;                    // [d][lp]
-  float* Ps = Xs + d * lp;           // [d][lp]
+  float* Ps = Xs + d * lp;           // [d][lp]; first Z^T [lp][d]
   float* Ts = Ps + d * lp;           // [lp][lp]
+  float* Ms = Ts + lp * lp;          // [2][kMRows][d]
   const int c = threadIdx.x;
+  const float* Mg = a.M + static_cast<int64_t>(i) * d * d;
   float* XT = a.X + rows_at(i, d, lp);
   if (kFromZ) {
-    load_square(Ts, a.T + static_cast<int64_t>(i) * lp * lp, lp);
-    __syncthreads();
+    stage_floats(Ps, a.Z + rows_at(i, d, lp), lp * d);
+    stage_floats(Ts, a.T + static_cast<int64_t>(i) * lp * lp, lp * lp);
+  }
+  cp_async_commit();                                       // group: Z^T, T
+  stage_floats(Ms, Mg, kMRows * d);
+  cp_async_commit();                                       // group: M rows 0..15
+  cp_async_wait<1>();
+  __syncthreads();
+  if (kFromZ) {
     if (c < d) {
       RowAcc xr;
       row_zero(xr);
-      row_times(a.Z + rows_at(i, d, lp), d, c, Ts, xr, l, lp);
+      row_times(Ps, d, c, Ts, xr, l, lp);
       row_store(xr, Xs + c * lp, XT, d, c, lp);
     }
   } else if (c < d) {
@@ -370,34 +400,41 @@ __global__ void __launch_bounds__(kRowThreads)
       XT[static_cast<int64_t>(j) * d + c] = v;
     }
   }
-  __syncthreads();
-  if (c < d) {
-    // P1 row c = sum_k M(c, k) X[k]; M(c, k) is column c of the stored
-    // (transposed) Gram, read 16 rows of k ahead
-    RowAcc acc;
-    row_zero(acc);
-    const float* Mc = a.M + static_cast<int64_t>(i) * d * d + c;
-    for (int kb = 0; kb < d; kb += 16) {
-      float mv[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) mv[u] = __ldg(Mc + (kb + u) * d);
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const float* xr = Xs + (kb + u) * lp;
+  // P1 row c = sum_k M(c, k) X[k]; M(c, k) is column c of the stored
+  // (transposed) Gram, i.e. Ms[k][c]
+  RowAcc acc;
+  row_zero(acc);
+  const int nblk = d / kMRows;
+  for (int kb = 0; kb < nblk; ++kb) {
+    if (kb + 1 < nblk) {
+      stage_floats(Ms + ((kb + 1) & 1) * kMRows * d, Mg + (kb + 1) * kMRows * d, kMRows * d);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();                                       // M block kb (and X) visible
+    if (c < d) {
+      const float* mb = Ms + (kb & 1) * kMRows * d;
+#pragma unroll 4
+      for (int u = 0; u < kMRows; ++u) {
+        const float m = mb[u * d + c];
+        const float* xr = Xs + (kb * kMRows + u) * lp;
 #pragma unroll
         for (int q4 = 0; q4 < kLmax / 4; ++q4) {
           if (4 * q4 < lp) {
             const float4 xv = *reinterpret_cast<const float4*>(xr + 4 * q4);
-            acc.v[q4].x = fmaf(mv[u], xv.x, acc.v[q4].x);
-            acc.v[q4].y = fmaf(mv[u], xv.y, acc.v[q4].y);
-            acc.v[q4].z = fmaf(mv[u], xv.z, acc.v[q4].z);
-            acc.v[q4].w = fmaf(mv[u], xv.w, acc.v[q4].w);
+            acc.v[q4].x = fmaf(m, xv.x, acc.v[q4].x);
+            acc.v[q4].y = fmaf(m, xv.y, acc.v[q4].y);
+            acc.v[q4].z = fmaf(m, xv.z, acc.v[q4].z);
+            acc.v[q4].w = fmaf(m, xv.w, acc.v[q4].w);
           }
         }
       }
     }
-    row_store(acc, Ps + c * lp, a.P1 + rows_at(i, d, lp), d, c, lp);
+    __syncthreads();                                       // stage kb & 1 is refilled next
   }
+  if (c < d) row_store(acc, Ps + c * lp, a.P1 + rows_at(i, d, lp), d, c, lp);
   __syncthreads();
   gram_blocks(Xs, Ps, a.G + static_cast<int64_t>(i) * lp * lp, d, lp);
 }
@@ -412,13 +449,17 @@ __global__ void __launch_bounds__(kRowThreads)
   extern __shared__ float sh[];
   float* Ts = sh;                    // [lp][lp]
   float* Zs = Ts + lp * lp;          // [d][lp]
+  float* PT = Zs + d * lp;           // P1^T [lp][d]
   const int c = threadIdx.x;
-  load_square(Ts, a.T + static_cast<int64_t>(i) * lp * lp, lp);
+  stage_floats(Ts, a.T + static_cast<int64_t>(i) * lp * lp, lp * lp);
+  stage_floats(PT, a.P1 + rows_at(i, d, lp), lp * d);
+  cp_async_commit();
+  cp_async_wait<0>();
   __syncthreads();
   if (c < d) {
     RowAcc zr;
     row_zero(zr);
-    row_times(a.P1 + rows_at(i, d, lp), d, c, Ts, zr, l, lp);
+    row_times(PT, d, c, Ts, zr, l, lp);
     row_store(zr, Zs + c * lp, a.Z + rows_at(i, d, lp), d, c, lp);
   }
   __syncthreads();
@@ -437,16 +478,21 @@ __global__ void __launch_bounds__(kRowThreads)
   float* Ts = sh;                    // R_Y^-1 [lp][lp]
   float* Us = Ts + lp * lp;          // Ub [lp][lp]
   float* ls_ = Us + lp * lp;         // lam [lp]
-  float* TtT = ls_ + lp;             // (X R_Y^-1) transposed [lp][d]
-  load_square(Ts, a.T + static_cast<int64_t>(i) * lp * lp, lp);
-  load_square(Us, a.Ub + static_cast<int64_t>(i) * lp * lp, lp);
-  for (int j = threadIdx.x; j < lp; j += blockDim.x) ls_[j] = a.lam[static_cast<int64_t>(i) * lp + j];
+  float* ZT = ls_ + lp;              // Z^T [lp][d]
+  float* XTs = ZT + lp * d;          // X^T [lp][d], then (X R_Y^-1)^T
+  stage_floats(Ts, a.T + static_cast<int64_t>(i) * lp * lp, lp * lp);
+  stage_floats(Us, a.Ub + static_cast<int64_t>(i) * lp * lp, lp * lp);
+  stage_floats(ls_, a.lam + static_cast<int64_t>(i) * lp, lp);
+  stage_floats(ZT, a.Z + rows_at(i, d, lp), lp * d);
+  stage_floats(XTs, a.X + rows_at(i, d, lp), lp * d);
+  cp_async_commit();
+  cp_async_wait<0>();
   __syncthreads();
   const int c = threadIdx.x;
   if (c >= d) return;
   RowAcc acc;
   row_zero(acc);
-  row_times(a.Z + rows_at(i, d, lp), d, c, Us, acc, l, lp);     // (Z Ub) row c
+  row_times(ZT, d, c, Us, acc, l, lp);                     // (Z Ub) row c
   const float sig_max = sqrtf(ls_[0]);
   __nv_bfloat16* Wo = reinterpret_cast<__nv_bfloat16*>(a.W[x.kv]) +
                       static_cast<int64_t>(x.unit) * d * a.A * r +
@@ -462,113 +508,220 @@ __global__ void __launch_bounds__(kRowThreads)
       Wo[j] = __float2bfloat16_rn(v);
     }
   }
-  // (X R_Y^-1) row c, kept transposed in shared memory, then P = that Ub_r diag(sigma_r)
+  // (X R_Y^-1) row c, written over this thread's column of X^T, then
+  // P = that Ub_r diag(sigma_r)
   row_zero(acc);
-  row_times(a.X + rows_at(i, d, lp), d, c, Ts, acc, l, lp);
+  row_times(XTs, d, c, Ts, acc, l, lp);
 #pragma unroll
   for (int j = 0; j < kLmax; ++j)
-    if (j < lp) TtT[j * d + c] = row_get(acc, j);
+    if (j < lp) XTs[j * d + c] = row_get(acc, j);
   row_zero(acc);
-  row_times(TtT, d, c, Us, acc, l, lp);
+  row_times(XTs, d, c, Us, acc, l, lp);
   float* Po = a.P + static_cast<int64_t>(i) * d * r + static_cast<int64_t>(c) * r;
 #pragma unroll
   for (int j = 0; j < kLmax; ++j)
     if (j < r) Po[j] = j < l ? row_get(acc, j) * sqrtf(ls_[j]) : 0.0f;
 }
 
-// U = delta P over the segment's rows (zero rows up to Tmax).  The exact and
-// reference rows stream through shared memory in 64-row tiles (cp.async,
-// 16-byte coalesced chunks, two stages, rows past the segment zero-filled);
-// thread = (row of the tile, a quarter of the r columns), delta formed in
-// fp32 from the bf16 pair, features summed in ascending order.  For pool
-// insertion (summaries != nullptr) the K matrix also writes the slot's
-// summary, the mean of the held keys.
-constexpr int kUTile = 64;
+// ===================================================================== U
+// U = delta P on tcgen05 over the segment's rows (zero rows up to Tmax).  Per
+// 128-token tile the exact and reference rows are read 16 bytes at a time
+// into registers (the next tile's reads are issued before the current tile's
+// MMAs), delta = exact - ref is formed in fp32 and split into bf16 hi + lo,
+// stored K-major (row = token, 64 features per 128-byte swizzled row).  P
+// (fp32 [d][r]) is split once per matrix into hi + lo rows of P^T (row = rank
+// column; rows r..Np-1 zero, Np = r rounded up to 16).  Three MMAs per
+// 16-feature step, hi.hi + hi.lo + lo.hi (the lo.lo term is below 2^-16 of
+// the product), M = 128 tokens, N = Np, alternate between two TMEM
+// accumulators, so tile k's epilogue (TMEM -> bf16 U rows) overlaps tile
+// k+1's MMAs.  For pool insertion (summaries != nullptr) the K matrix also
+// writes the slot's summary, the mean of the held keys.
+constexpr int kUTok = 128;
+constexpr int kUAtom = kUTok * 128;           // one 64-feature atom of a tile (16 KB)
+constexpr uint32_t kUCols = 128;              // two accumulators of up to 64 columns
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n)
-               : "memory");
+struct UTileRegs {
+  uint4 e[8], r[8];
+};
+
+__device__ __forceinline__ void u_load(UTileRegs& t, const __nv_bfloat16* ex,
+                                       const __nv_bfloat16* rf, int64_t es3, int64_t rs3,
+                                       int tile, int n, int d) {
+  const int cpr = d >> 3;                     // 16-byte chunks per row
+  const int nq = (kUTok * cpr) / kUThreads;   // 8 (d = 128) or 4 (d = 64)
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    if (s < nq) {
+      const int q = threadIdx.x + s * kUThreads;
+      const int row = q / cpr, ch = q - row * cpr;
+      const int tk = tile * kUTok + row;
+      const bool in = tk < n;
+      t.e[s] = in ? *reinterpret_cast<const uint4*>(ex + tk * es3 + ch * 8) : make_uint4(0, 0, 0, 0);
+      t.r[s] = in ? *reinterpret_cast<const uint4*>(rf + tk * rs3 + ch * 8) : make_uint4(0, 0, 0, 0);
+    }
+  }
 }
 
-__global__ void __launch_bounds__(kUThreads)
+__device__ __forceinline__ void u_store(const UTileRegs& t, uint8_t* Ahi, uint8_t* Alo, int d) {
+  const int cpr = d >> 3;
+  const int nq = (kUTok * cpr) / kUThreads;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    if (s < nq) {
+      const int q = threadIdx.x + s * kUThreads;
+      const int row = q / cpr, ch = q - row * cpr;
+      const int off = (ch >> 3) * kUAtom + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+      const __nv_bfloat162* e2 = reinterpret_cast<const __nv_bfloat162*>(&t.e[s]);
+      const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&t.r[s]);
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const float2 ef = __bfloat1622float2(e2[p]), rv = __bfloat1622float2(r2[p]);
+        const float d0 = ef.x - rv.x, d1 = ef.y - rv.y;
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(d0, d1);
+        const float2 hf = __bfloat1622float2(hb);
+        const __nv_bfloat162 lb = __floats2bfloat162_rn(d0 - hf.x, d1 - hf.y);
+        hw[p] = *reinterpret_cast<const uint32_t*>(&hb);
+        lw[p] = *reinterpret_cast<const uint32_t*>(&lb);
+      }
+      *reinterpret_cast<uint4*>(Ahi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(Alo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kUThreads, 2)
     u_kernel(const StageArgs a, const __grid_constant__ SegTable seg) {
   const int i = blockIdx.x;
   const Mat x = decode_mat(a, seg, a.m0 + i);
-  if (x.skip) return;
-  const int d = a.d, r = a.r;
-  const int rowB = d * 2 + 16;                              // padded tile row (bytes)
-  extern __shared__ float sh[];
-  float* Ps = sh;                                           // [d][r]
-  uint8_t* tiles = reinterpret_cast<uint8_t*>(Ps + d * r);  // [2 stages][exact, ref][kUTile][rowB]
-  const int stageB = 2 * kUTile * rowB;
-  const float* Pg = a.P + static_cast<int64_t>(i) * d * r;
-  for (int idx = threadIdx.x; idx < d * r; idx += blockDim.x) Ps[idx] = Pg[idx];
+  if (x.skip) return;                                       // uniform per CTA
+  const int d = a.d, r = a.r, Np = (r + 15) & ~15;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Ahi = sm;                                        // [2 atoms][128 tokens][128 B]
+  uint8_t* Alo = Ahi + 2 * kUAtom;
+  uint8_t* Bhi = Alo + 2 * kUAtom;                          // [2 atoms][Np rows][128 B]
+  uint8_t* Blo = Bhi + 2 * Np * 128;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(Blo + 2 * Np * 128);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mbar + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(mbar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc<kUCols>(tmem_slot);
+    tmem_relinquish();
+  }
   const __nv_bfloat16* ex = rows_of(a.exact[x.kv], a.es[x.kv], seg, x);
   const __nv_bfloat16* rf = rows_of(a.ref[x.kv], a.rs[x.kv], seg, x);
   const int64_t es3 = a.es[x.kv][3], rs3 = a.rs[x.kv][3];
-  const int chunks = d / 8;                                 // 16-byte chunks per row
-  const int ntiles = (a.Tmax + kUTile - 1) / kUTile;
-  auto issue = [&](int tile, int stage) {
-    uint8_t* te = tiles + stage * stageB;
-    uint8_t* tr = te + kUTile * rowB;
-    for (int q = threadIdx.x; q < kUTile * chunks; q += blockDim.x) {
-      const int row = q / chunks, ch = q - (q / chunks) * chunks;
-      const int t = tile * kUTile + row;
-      const bool in = t < x.n;
-      const int ts = in ? t : 0;
-      cp_async16(te + row * rowB + ch * 16, ex + ts * es3 + ch * 8, in);
-      cp_async16(tr + row * rowB + ch * 16, rf + ts * rs3 + ch * 8, in);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  };
-  issue(0, 0);
-  const int row = threadIdx.x >> 2;                         // 0..63
-  const int jw = r >> 2;                                    // columns per thread (r % 8 == 0)
-  const int j0 = (threadIdx.x & 3) * jw;
+  const int ntiles = (a.Tmax + kUTok - 1) / kUTok;
+  UTileRegs tr;
+  u_load(tr, ex, rf, es3, rs3, 0, x.n, d);
+  // P^T hi / lo (j fastest, so the reads of P rows are contiguous)
+  const float* Pg = a.P + static_cast<int64_t>(i) * d * r;
+  for (int idx = threadIdx.x; idx < Np * d; idx += kUThreads) {
+    const int c = idx / Np, j = idx - c * Np;
+    const float v = j < r ? Pg[c * r + j] : 0.0f;
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(h));
+    const int cc = c & 63;
+    const int off = (c >> 6) * (Np * 128) + j * 128 + ((((cc >> 3) ^ (j & 7))) << 4) + (cc & 7) * 2;
+    *reinterpret_cast<__nv_bfloat16*>(Bhi + off) = h;
+    *reinterpret_cast<__nv_bfloat16*>(Blo + off) = lo;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t idesc = idesc_bf16_f32(kUTok, Np);
   __nv_bfloat16* Uo = reinterpret_cast<__nv_bfloat16*>(a.U[x.kv]) +
                       static_cast<int64_t>(x.unit) * a.Tmax * a.A * r;
-  for (int tile = 0; tile < ntiles; ++tile) {
-    const int stage = tile & 1;
-    if (tile + 1 < ntiles) {
-      issue(tile + 1, stage ^ 1);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    } else {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-    }
-    __syncthreads();
-    const uint8_t* te = tiles + stage * stageB + row * rowB;
-    const uint8_t* tr = te + kUTile * rowB;
-    float acc[kLmax / 4];
+  const int qd = warp & 3, half = warp >> 2;
+  // TMEM accumulator of tile kt -> bf16 U rows (warp quadrant = 32 tokens,
+  // the two warp halves take alternate 16-column blocks)
+  auto epilogue = [&](int kt) {
+    const int row = kt * kUTok + qd * 32 + lane;
+    for (int cb = half; cb * 16 < Np; cb += 2) {
+      uint32_t v[16];
+      __syncwarp();
+      tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(qd * 32) << 16) + (kt & 1) * Np + cb * 16,
+                         v);
+      tmem_ld_wait();
+      if (row < a.Tmax) {
+        __nv_bfloat16* urow = Uo + (static_cast<int64_t>(row) * a.A + x.slot) * r + cb * 16;
 #pragma unroll
-    for (int jj = 0; jj < kLmax / 4; ++jj) acc[jj] = 0.0f;
-#pragma unroll 2
-    for (int c = 0; c < d; c += 2) {
-      const float2 e2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(te + c * 2));
-      const float2 r2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(tr + c * 2));
-      const float d0 = e2.x - r2.x, d1 = e2.y - r2.y;
-      const float* p0 = Ps + c * r + j0;
-      const float* p1 = p0 + r;
+        for (int h = 0; h < 2; ++h) {
+          if (cb * 16 + 8 * h < r) {
+            uint32_t w4[4];
 #pragma unroll
-      for (int jj = 0; jj < kLmax / 4; ++jj) {
-        if (jj < jw) {
-          acc[jj] = fmaf(d0, p0[jj], acc[jj]);
-          acc[jj] = fmaf(d1, p1[jj], acc[jj]);
+            for (int p = 0; p < 4; ++p) {
+              const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[8 * h + 2 * p]),
+                                                             __uint_as_float(v[8 * h + 2 * p + 1]));
+              w4[p] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            *reinterpret_cast<uint4*>(urow + 8 * h) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
         }
       }
     }
-    const int t = tile * kUTile + row;
-    if (t < a.Tmax) {
-      __nv_bfloat16* urow = Uo + (static_cast<int64_t>(t) * a.A + x.slot) * r + j0;
-#pragma unroll
-      for (int jj = 0; jj < kLmax / 4; jj += 2)
-        if (jj < jw)
-          *reinterpret_cast<__nv_bfloat162*>(urow + jj) = __floats2bfloat162_rn(acc[jj], acc[jj + 1]);
+    tc_fence_before();
+  };
+  bool ok = true;
+  int committed = 0;                                        // tiles whose MMAs were issued
+  for (int k = 0; k < ntiles; ++k) {
+    if (k >= 1) {                                           // tile k-1's MMAs read the A buffer
+      const bool got = threadIdx.x != 0 || mbar_wait_bounded(mbar, (k - 1) & 1, kWaitLimitNs);
+      if (!__syncthreads_and(got)) {
+        if (threadIdx.x == 0) atomicCAS(a.dev_status, 0, static_cast<int32_t>(KVC_ERR_DEVICE_TIMEOUT));
+        ok = false;
+        break;
+      }
+      tc_fence_after();
     }
-    __syncthreads();                                        // the stage is refilled two tiles on
+    u_store(tr, Ahi, Alo, d);
+    if (k + 1 < ntiles) u_load(tr, ex, rf, es3, rs3, k + 1, x.n, d);
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+      const uint32_t acc = tmem + (k & 1) * Np;
+      const uint32_t ah0 = smem_u32(Ahi), al0 = smem_u32(Alo);
+      const uint32_t bh0 = smem_u32(Bhi), bl0 = smem_u32(Blo);
+      for (int ks = 0; ks < d / 16; ++ks) {
+        const uint32_t ao = (ks >> 2) * kUAtom + (ks & 3) * 32;
+        const uint32_t bo = (ks >> 2) * (Np * 128) + (ks & 3) * 32;
+        const uint64_t ah = desc_kmajor_sw128(ah0 + ao), al = desc_kmajor_sw128(al0 + ao);
+        const uint64_t bh = desc_kmajor_sw128(bh0 + bo), bl = desc_kmajor_sw128(bl0 + bo);
+        mma_bf16_ss(acc, ah, bh, idesc, ks != 0 ? 1u : 0u);
+        mma_bf16_ss(acc, ah, bl, idesc, 1u);
+        mma_bf16_ss(acc, al, bh, idesc, 1u);
+      }
+      mma_commit(mbar);
+    }
+    committed = k + 1;
+    if (k >= 1) epilogue(k - 1);
   }
-  if (a.summaries != nullptr && x.kv == 0) {
+  if (ok && committed == ntiles && ntiles > 0) {
+    const bool got = threadIdx.x != 0 || mbar_wait_bounded(mbar, (ntiles - 1) & 1, kWaitLimitNs);
+    if (__syncthreads_and(got)) {
+      tc_fence_after();
+      epilogue(ntiles - 1);
+    } else {
+      if (threadIdx.x == 0) atomicCAS(a.dev_status, 0, static_cast<int32_t>(KVC_ERR_DEVICE_TIMEOUT));
+      ok = false;
+    }
+  } else if (!ok && threadIdx.x == 0 && committed > 0) {
+    // MMAs still in flight after an abort finish before TMEM is freed
+    (void)mbar_wait_bounded(mbar, (committed - 1) & 1, kWaitLimitNs);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc<kUCols>(tmem);
+  if (ok && a.summaries != nullptr && x.kv == 0) {
     float* smy = a.summaries + (static_cast<int64_t>(x.unit) * a.A + x.slot) * d;
     for (int c = threadIdx.x; c < d; c += blockDim.x) {
       float acc = 0.0f;
@@ -623,11 +776,10 @@ cudaError_t run_passes(StageArgs& a, const SegTable& seg, int64_t mats, int64_t 
                        const DeviceInfo& di, cudaStream_t stream) {
   const int d = a.d, lp = a.lp, r = a.r, l = a.l;
   const size_t gram_smem = 1024 + 2 * 2 * kDP * 128 + 64 + 64;
-  const size_t mx_smem = static_cast<size_t>(2 * d * lp + lp * lp) * sizeof(float);
-  const size_t zg_smem = static_cast<size_t>(lp * lp + d * lp) * sizeof(float);
-  const size_t wp_smem = static_cast<size_t>(2 * lp * lp + lp + lp * d) * sizeof(float);
-  const size_t u_smem = static_cast<size_t>(d * r) * sizeof(float) +
-                        static_cast<size_t>(2 * 2 * kUTile) * (d * 2 + 16);
+  const size_t mx_smem = static_cast<size_t>(2 * d * lp + lp * lp + 2 * kMRows * d) * sizeof(float);
+  const size_t zg_smem = static_cast<size_t>(lp * lp + 2 * d * lp) * sizeof(float);
+  const size_t wp_smem = static_cast<size_t>(2 * lp * lp + lp + 2 * lp * d) * sizeof(float);
+  const size_t u_smem = 1024 + 4 * kUAtom + 4 * static_cast<size_t>((r + 15) & ~15) * 128 + 64;
   const size_t chol_smem = chol_smem_bytes(false, l);
   const size_t qr2_smem = chol_smem_bytes(true, l);
   const size_t eig_smem = eig_smem_bytes(l);
