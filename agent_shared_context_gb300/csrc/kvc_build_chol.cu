@@ -143,23 +143,58 @@ __device__ void tri_inv_inplace(float* __restrict__ A, const int* keep, const fl
   __syncwarp();
 }
 
-// C = op(A) B, column-major l x l (stride cs), op(A) = A or A^T; lane k
-// computes its columns, t ascending.
-__device__ void cmm(const float* __restrict__ A, bool transA, const float* __restrict__ B,
-                    float* __restrict__ C, int l, int cs, int lane) {
-  for (int k = lane; k < l; k += 32) {
-    const float* bk = B + k * cs;
-    for (int m = 0; m < l; ++m) {
+// Products with the upper-triangular factors of CholeskyQR2, in place
+// (column-major, stride cs).  Each sum runs t ascending and skips only terms
+// whose triangular factor is an exact zero, so the results equal the full
+// products bit for bit.
+//
+// A <- A Ri, Ri upper triangular: row m of the result depends on row m of A
+// only, so lane m rewrites its rows, columns k descending:
+// A[m][k] = sum_{t <= k} A[m][t] Ri[t][k].
+__device__ void right_mul_upper(float* __restrict__ A, const float* __restrict__ Ri, int l,
+                                int cs, int lane) {
+  for (int m = lane; m < l; m += 32) {
+    for (int k = l - 1; k >= 0; --k) {
+      const float* rk = Ri + k * cs;
       float acc = 0.0f;
-      if (transA) {
-        const float* am = A + m * cs;              // column m of A = row m of A^T
 #pragma unroll 4
-        for (int t = 0; t < l; ++t) acc = fmaf(am[t], bk[t], acc);
-      } else {
+      for (int t = 0; t <= k; ++t) acc = fmaf(A[t * cs + m], rk[t], acc);
+      A[k * cs + m] = acc;
+    }
+  }
+  __syncwarp();
+}
+
+// Upper triangle of Ri^T H in place of H: column k of the result depends on
+// column k of H only, so lane k rewrites its columns, rows m descending:
+// H[m][k] = sum_{t <= m} Ri[t][m] H[t][k] (m <= k).
+__device__ void left_mul_upper_t(const float* __restrict__ Ri, float* __restrict__ H, int l,
+                                 int cs, int lane) {
+  for (int k = lane; k < l; k += 32) {
+    float* hk = H + k * cs;
+    for (int m = k; m >= 0; --m) {
+      const float* rm = Ri + m * cs;
+      float acc = 0.0f;
 #pragma unroll 4
-        for (int t = 0; t < l; ++t) acc = fmaf(A[t * cs + m], bk[t], acc);
-      }
-      C[k * cs + m] = acc;
+      for (int t = 0; t <= m; ++t) acc = fmaf(rm[t], hk[t], acc);
+      hk[m] = acc;
+    }
+  }
+  __syncwarp();
+}
+
+// A <- A B, both upper triangular: lane m rewrites its rows, columns k
+// descending: A[m][k] = sum_{m <= t <= k} A[m][t] B[t][k]; zero below the
+// diagonal stays zero.
+__device__ void right_mul_upper_upper(float* __restrict__ A, const float* __restrict__ B, int l,
+                                      int cs, int lane) {
+  for (int m = lane; m < l; m += 32) {
+    for (int k = l - 1; k >= m; --k) {
+      const float* bk = B + k * cs;
+      float acc = 0.0f;
+#pragma unroll 4
+      for (int t = m; t <= k; ++t) acc = fmaf(A[t * cs + m], bk[t], acc);
+      A[k * cs + m] = acc;
     }
   }
   __syncwarp();
@@ -203,7 +238,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
   const int l = a.l, lp = a.lp, cs = col_stride(l);
   extern __shared__ float sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const WarpMats w = warp_mats(sh, warp, l, kQr2 ? 3 : 1);
+  const WarpMats w = warp_mats(sh, warp, l, kQr2 ? 2 : 1);
   const int i = blockIdx.x * kSmallWarps + warp;
   if (i >= a.nm) return;
   const Mat x = decode_mat(a, seg, a.m0 + i);
@@ -221,12 +256,12 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
   __syncwarp();
   chol_inplace(w.B, w.keep, w.dinv, w.diag, w.lam, l, cs, lane);     // R1             (B)
   tri_inv_inplace(w.B, w.keep, w.diag, l, cs, lane);                 // Ri1            (B)
-  cmm(w.A, false, w.B, w.C, l, cs, lane);                            // H = G Ri1      (C)
-  cmm(w.B, true, w.C, w.A, l, cs, lane);                             // G2 = Ri1^T H   (A)
+  right_mul_upper(w.A, w.B, l, cs, lane);                            // H = G Ri1      (A)
+  left_mul_upper_t(w.B, w.A, l, cs, lane);                           // G2 = Ri1^T H   (A)
   chol_inplace(w.A, w.keep, w.dinv, w.diag, w.lam, l, cs, lane);     // R2             (A)
   tri_inv_inplace(w.A, w.keep, w.diag, l, cs, lane);                 // Ri2            (A)
-  cmm(w.B, false, w.A, w.C, l, cs, lane);                            // R_Y^-1 = Ri1 Ri2 (C)
-  const float* out = w.C;
+  right_mul_upper_upper(w.B, w.A, l, cs, lane);                      // R_Y^-1 = Ri1 Ri2 (B)
+  const float* out = w.B;
   store_cols(out, a.T + static_cast<int64_t>(i) * lp * lp, l, lp, cs, lane);
 }
 
@@ -381,7 +416,7 @@ size_t smem_bytes(int l, int nmats) {
 
 }  // namespace
 
-size_t chol_smem_bytes(bool qr2, int l) { return smem_bytes(l, qr2 ? 3 : 1); }
+size_t chol_smem_bytes(bool qr2, int l) { return smem_bytes(l, qr2 ? 2 : 1); }
 size_t eig_smem_bytes(int l) { return smem_bytes(l, 1); }
 
 cudaError_t launch_chol(const StageArgs& a, const SegTable& seg, bool qr2, int grid, size_t smem,

@@ -332,6 +332,31 @@ __device__ __forceinline__ void row_times(const float* inT, int d, int c, const 
   }
 }
 
+// The same product with Ts upper triangular (the inverse Cholesky factors):
+// column block q4 of the result only sums rows t < 4 q4 + 4 of Ts (the rest
+// are exact zeros), in the same ascending order, so the result equals
+// row_times bit for bit with about half the work.
+__device__ __forceinline__ void row_times_upper(const float* inT, int d, int c, const float* Ts,
+                                                RowAcc& acc, int l, int lp) {
+#pragma unroll
+  for (int q4 = 0; q4 < kLmax / 4; ++q4) {
+    if (4 * q4 < lp) {
+      const int tn = min(l, 4 * q4 + 4);
+      float4 s = acc.v[q4];
+#pragma unroll 4
+      for (int t = 0; t < tn; ++t) {
+        const float v = inT[t * d + c];
+        const float4 b = *reinterpret_cast<const float4*>(Ts + t * lp + 4 * q4);
+        s.x = fmaf(v, b.x, s.x);
+        s.y = fmaf(v, b.y, s.y);
+        s.z = fmaf(v, b.z, s.z);
+        s.w = fmaf(v, b.w, s.w);
+      }
+      acc.v[q4] = s;
+    }
+  }
+}
+
 // Store a row to shared memory (row-major, stride lp) and to the transposed
 // global array.
 __device__ __forceinline__ void row_store(const RowAcc& acc, float* rs, float* gT, int d, int c,
@@ -390,7 +415,7 @@ __global__ void __launch_bounds__(kRowThreads)
     if (c < d) {
       RowAcc xr;
       row_zero(xr);
-      row_times(Ps, d, c, Ts, xr, l, lp);
+      row_times_upper(Ps, d, c, Ts, xr, l, lp);
       row_store(xr, Xs + c * lp, XT, d, c, lp);
     }
   } else if (c < d) {
@@ -459,7 +484,7 @@ __global__ void __launch_bounds__(kRowThreads)
   if (c < d) {
     RowAcc zr;
     row_zero(zr);
-    row_times(PT, d, c, Ts, zr, l, lp);
+    row_times_upper(PT, d, c, Ts, zr, l, lp);
     row_store(zr, Zs + c * lp, a.Z + rows_at(i, d, lp), d, c, lp);
   }
   __syncthreads();
@@ -511,7 +536,7 @@ __global__ void __launch_bounds__(kRowThreads)
   // (X R_Y^-1) row c, written over this thread's column of X^T, then
   // P = that Ub_r diag(sigma_r)
   row_zero(acc);
-  row_times(XTs, d, c, Ts, acc, l, lp);
+  row_times_upper(XTs, d, c, Ts, acc, l, lp);
 #pragma unroll
   for (int j = 0; j < kLmax; ++j)
     if (j < lp) XTs[j * d + c] = row_get(acc, j);
@@ -620,17 +645,41 @@ __global__ void __launch_bounds__(kUThreads, 2)
   const int ntiles = (a.Tmax + kUTok - 1) / kUTok;
   UTileRegs tr;
   u_load(tr, ex, rf, es3, rs3, 0, x.n, d);
-  // P^T hi / lo (j fastest, so the reads of P rows are contiguous)
-  const float* Pg = a.P + static_cast<int64_t>(i) * d * r;
-  for (int idx = threadIdx.x; idx < Np * d; idx += kUThreads) {
-    const int c = idx / Np, j = idx - c * Np;
-    const float v = j < r ? Pg[c * r + j] : 0.0f;
-    const __nv_bfloat16 h = __float2bfloat16_rn(v);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(h));
-    const int cc = c & 63;
-    const int off = (c >> 6) * (Np * 128) + j * 128 + ((((cc >> 3) ^ (j & 7))) << 4) + (cc & 7) * 2;
-    *reinterpret_cast<__nv_bfloat16*>(Bhi + off) = h;
-    *reinterpret_cast<__nv_bfloat16*>(Blo + off) = lo;
+  // P^T hi / lo: thread = (feature c, 4 adjacent rank columns), all its
+  // 16-byte reads of P issued before the shared-memory stores
+  {
+    const float* Pg = a.P + static_cast<int64_t>(i) * d * r;
+    const int g4 = Np >> 2;                                 // column groups per feature
+    const int n4 = g4 * d;                                  // <= 16 * 128 = 2048
+    for (int base = 0; base < n4; base += 4 * kUThreads) {
+      float4 pv[4];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int idx = base + threadIdx.x + s * kUThreads;
+        const int c = idx / g4, j0 = 4 * (idx - (idx / g4) * g4);
+        pv[s] = (idx < n4 && j0 < r) ? *reinterpret_cast<const float4*>(Pg + c * r + j0)
+                                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int idx = base + threadIdx.x + s * kUThreads;
+        if (idx < n4) {
+          const int c = idx / g4, j0 = 4 * (idx - (idx / g4) * g4);
+          const int cc = c & 63;
+          const float v4[4] = {pv[s].x, pv[s].y, pv[s].z, pv[s].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j0 + u;
+            const __nv_bfloat16 h = __float2bfloat16_rn(v4[u]);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(v4[u] - __bfloat162float(h));
+            const int off =
+                (c >> 6) * (Np * 128) + j * 128 + (((cc >> 3) ^ (j & 7)) << 4) + (cc & 7) * 2;
+            *reinterpret_cast<__nv_bfloat16*>(Bhi + off) = h;
+            *reinterpret_cast<__nv_bfloat16*>(Blo + off) = lo;
+          }
+        }
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();

@@ -378,9 +378,14 @@ def _builder_leg(args, dev, wl=None):
     peak, peak_kind = _peaks()
     tflops = gemm_flop / (b_ms / 1000.0) / 1e12
     b_gbs = b_bytes / (b_ms / 1000.0) / 1e9
-    tc = wl.d <= 128 and l <= 64
-    out = {"workload": wl.name, "kernel": "build_tc_kernel" if tc else "build_simt_kernel",
-           "launch_ms": b_ms, "matrices": mats, "matrix": "%d x %d" % (wl.max_seg_len, wl.d),
+    if wl.dtype == "bf16" and wl.d in (64, 128) and l <= 64:
+        kernel = ("staged builder: gram_kernel, mx_kernel, chol_kernel, zg_kernel, eig_kernel, "
+                  "wp_kernel, u_kernel per pass of up to 8,192 matrices")
+    elif wl.d <= 128 and l <= 64:
+        kernel = "build_tc_kernel"
+    else:
+        kernel = "build_simt_kernel"
+    out = {"workload": wl.name, "kernel": kernel, "launch_ms": b_ms, "ms_per_edge": b_ms, "matrices": mats, "matrix": "%d x %d" % (wl.max_seg_len, wl.d),
            "hmt_gemm_equivalent_tflops": tflops,
            "tensor_frac_of_bf16_peak": tflops / bf16_pk, "bf16_peak_tflops": bf16_pk,
            "bf16_peak_kind": bf16_kind,
@@ -443,7 +448,17 @@ def run_kvc(args, wl):
     for _ in range(max(args.warmup, 3)):
         runner.run()
     torch.cuda.synchronize(dev)
-    launches_per_step = wl.edges * (4 + (1 if runner.build else 0) + (1 if runner.rank_mode else 0))
+    # per edge: match, apply, segment reduce, fallback copy (+ the rank-r_C
+    # representations); a state build adds the staged builder's 4 q + 7
+    # kernels per pass of up to 8,192 matrices (one kernel on other paths)
+    build_launches = 0
+    if runner.build:
+        if wl.dtype == "bf16" and wl.d in (64, 128) and wl.l <= 64:
+            passes = -(-(wl.S * wl.L * wl.H * 2) // 8192)
+            build_launches = passes * (4 * wl.power_iters + 7)
+        else:
+            build_launches = 1
+    launches_per_step = wl.edges * (4 + build_launches + (1 if runner.rank_mode else 0))
 
     barrier()
     torch.cuda.synchronize(dev)
