@@ -25,6 +25,9 @@ struct WarpMats {
   float* A;        // column-major scratch (cs x l)
   float* B;        // column-major scratch (cs x l)
   float* C;        // column-major scratch (cs x l)
+  float* prow;     // [kLmax] the scaled pivot row of a Cholesky step (shares
+                   // its storage with order, which only the eigen stage's
+                   // final sort uses, after its Cholesky)
   int* keep;       // [kLmax]
   float* dinv;     // [kLmax]
   float* diag;     // [kLmax]
@@ -34,22 +37,26 @@ struct WarpMats {
 
 __device__ __forceinline__ int col_stride(int l) { return l | 1; }
 
-__device__ __forceinline__ size_t warp_floats(int l, int nmats) {
-  return static_cast<size_t>(nmats) * col_stride(l) * l + 5 * kLmax;
+// Floats per warp: the matrices (rounded up to a multiple of 4) and five
+// vectors of kLmax.
+__host__ __device__ __forceinline__ size_t warp_floats(int l, int nmats) {
+  return ((static_cast<size_t>(nmats) * (l | 1) * l + 3) & ~static_cast<size_t>(3)) + 5 * kLmax;
 }
 
 __device__ __forceinline__ WarpMats warp_mats(float* sh, int warp, int l, int nmats) {
   const int cs = col_stride(l);
   float* base = sh + warp * warp_floats(l, nmats);
+  const size_t mats = (static_cast<size_t>(nmats) * cs * l + 3) & ~static_cast<size_t>(3);
   WarpMats w;
   w.A = base;
   w.B = nmats > 1 ? base + cs * l : nullptr;
   w.C = nmats > 2 ? base + 2 * cs * l : nullptr;
-  w.keep = reinterpret_cast<int*>(base + nmats * cs * l);
+  w.keep = reinterpret_cast<int*>(base + mats);
   w.dinv = reinterpret_cast<float*>(w.keep + kLmax);
   w.diag = w.dinv + kLmax;
   w.lam = w.diag + kLmax;
   w.order = reinterpret_cast<int*>(w.lam + kLmax);
+  w.prow = reinterpret_cast<float*>(w.order);
   return w;
 }
 
@@ -61,7 +68,7 @@ __device__ __forceinline__ WarpMats warp_mats(float* sh, int warp, int l, int nm
 // rows below j only, so every lane may read row j of the other columns while
 // the step runs.  gd is scratch for G's diagonal; diag gets the final R[i][i].
 __device__ void chol_inplace(float* __restrict__ A, int* keep, float* dinv, float* diag,
-                             float* gd, int l, int cs, int lane) {
+                             float* gd, float* prow, int l, int cs, int lane) {
   for (int k = lane; k < l; k += 32) {
     gd[k] = A[k * cs + k];
     for (int m = k + 1; m < l; ++m) A[k * cs + m] = 0.0f;
@@ -76,6 +83,10 @@ __device__ void chol_inplace(float* __restrict__ A, int* keep, float* dinv, floa
       keep[j] = ok ? 1 : 0;
       dinv[j] = ok ? rsqrtf(piv) : 0.0f;
     }
+    // row j of R scaled by -1 / pivot, contiguous (row j is not written in
+    // step j, and the previous step's readers finished at its barrier)
+    for (int i = j + 1 + lane; i < l; i += 32) prow[i] = -A[i * cs + j] * inv2;
+    __syncwarp();
     for (int k = lane; k < l; k += 32) {
       if (k <= j) continue;
       float* rk = A + k * cs;
@@ -86,13 +97,13 @@ __device__ void chol_inplace(float* __restrict__ A, int* keep, float* dinv, floa
         float t[8], v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          t[u] = A[(i + u) * cs + j];
+          t[u] = prow[i + u];
           v[u] = rk[i + u];
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) rk[i + u] = fmaf(-t[u] * inv2, rjk, v[u]);
+        for (int u = 0; u < 8; ++u) rk[i + u] = fmaf(t[u], rjk, v[u]);
       }
-      for (; i <= k; ++i) rk[i] = fmaf(-A[i * cs + j] * inv2, rjk, rk[i]);
+      for (; i <= k; ++i) rk[i] = fmaf(prow[i], rjk, rk[i]);
     }
     __syncwarp();
   }
@@ -239,13 +250,13 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
   extern __shared__ float sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WarpMats w = warp_mats(sh, warp, l, kQr2 ? 2 : 1);
-  const int i = blockIdx.x * kSmallWarps + warp;
+  const int i = blockIdx.x * static_cast<int>(blockDim.x >> 5) + warp;
   if (i >= a.nm) return;
   const Mat x = decode_mat(a, seg, a.m0 + i);
   if (x.skip) return;
   if (!kQr2) {
     load_gram(a.G + static_cast<int64_t>(i) * lp * lp, w.A, l, lp, cs, lane);
-    chol_inplace(w.A, w.keep, w.dinv, w.diag, w.lam, l, cs, lane);   // R      (A)
+    chol_inplace(w.A, w.keep, w.dinv, w.diag, w.lam, w.prow, l, cs, lane);   // R      (A)
     tri_inv_inplace(w.A, w.keep, w.diag, l, cs, lane);               // R^-1   (A)
     store_cols(w.A, a.T + static_cast<int64_t>(i) * lp * lp, l, lp, cs, lane);
     return;
@@ -254,11 +265,11 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
   for (int k = lane; k < l; k += 32)                                // G kept in A
     for (int m = 0; m < l; ++m) w.B[k * cs + m] = w.A[k * cs + m];
   __syncwarp();
-  chol_inplace(w.B, w.keep, w.dinv, w.diag, w.lam, l, cs, lane);     // R1             (B)
+  chol_inplace(w.B, w.keep, w.dinv, w.diag, w.lam, w.prow, l, cs, lane);     // R1             (B)
   tri_inv_inplace(w.B, w.keep, w.diag, l, cs, lane);                 // Ri1            (B)
   right_mul_upper(w.A, w.B, l, cs, lane);                            // H = G Ri1      (A)
   left_mul_upper_t(w.B, w.A, l, cs, lane);                           // G2 = Ri1^T H   (A)
-  chol_inplace(w.A, w.keep, w.dinv, w.diag, w.lam, l, cs, lane);     // R2             (A)
+  chol_inplace(w.A, w.keep, w.dinv, w.diag, w.lam, w.prow, l, cs, lane);     // R2             (A)
   tri_inv_inplace(w.A, w.keep, w.diag, l, cs, lane);                 // Ri2            (A)
   right_mul_upper_upper(w.B, w.A, l, cs, lane);                      // R_Y^-1 = Ri1 Ri2 (B)
   const float* out = w.B;
@@ -285,12 +296,12 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
   extern __shared__ float sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WarpMats w = warp_mats(sh, warp, l, 1);
-  const int i = blockIdx.x * kSmallWarps + warp;
+  const int i = blockIdx.x * static_cast<int>(blockDim.x >> 5) + warp;
   if (i >= a.nm) return;
   const Mat x = decode_mat(a, seg, a.m0 + i);
   if (x.skip) return;
   load_gram(a.G + static_cast<int64_t>(i) * lp * lp, w.A, l, lp, cs, lane);
-  chol_inplace(w.A, w.keep, w.dinv, w.diag, w.lam, l, cs, lane);
+  chol_inplace(w.A, w.keep, w.dinv, w.diag, w.lam, w.prow, l, cs, lane);
   float* Y = w.A;                 // y_p[e] = R[p][e] = Y[e * cs + p]
   float* nrm = w.diag;            // |y_p|^2: exact at each sweep's start, then tracked
   for (int sweep = 0; sweep < kSweepsOneSided; ++sweep) {
@@ -409,41 +420,36 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
   }
 }
 
+// Warps (one matrix each) per CTA: four for the one-array stages (28 warps
+// per SM at l = 40), three for CholeskyQR2, whose two arrays per warp make
+// shared memory the limit (15 warps per SM instead of 12 with four).
+int warps_per_cta(int nmats) { return nmats > 1 ? 3 : kSmallWarps; }
+
 size_t smem_bytes(int l, int nmats) {
-  return static_cast<size_t>(kSmallWarps) *
-         (static_cast<size_t>(nmats) * (l | 1) * l + 5 * kLmax) * sizeof(float);
+  return static_cast<size_t>(warps_per_cta(nmats)) * warp_floats(l, nmats) * sizeof(float);
+}
+
+template <typename K>
+cudaError_t launch_small(K kernel, const StageArgs& a, const SegTable& seg, int nmats,
+                         cudaStream_t stream) {
+  const int wpc = warps_per_cta(nmats);
+  const size_t smem = smem_bytes(a.l, nmats);
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kernel<<<(a.nm + wpc - 1) / wpc, wpc * 32, smem, stream>>>(a, seg);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t chol_smem_bytes(bool qr2, int l) { return smem_bytes(l, qr2 ? 2 : 1); }
-size_t eig_smem_bytes(int l) { return smem_bytes(l, 1); }
-
-cudaError_t launch_chol(const StageArgs& a, const SegTable& seg, bool qr2, int grid, size_t smem,
-                        cudaStream_t stream) {
-  const int threads = kSmallWarps * 32;
-  cudaError_t e;
-  if (qr2) {
-    if ((e = cudaFuncSetAttribute(chol_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(smem))) != cudaSuccess)
-      return e;
-    chol_kernel<true><<<grid, threads, smem, stream>>>(a, seg);
-  } else {
-    if ((e = cudaFuncSetAttribute(chol_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(smem))) != cudaSuccess)
-      return e;
-    chol_kernel<false><<<grid, threads, smem, stream>>>(a, seg);
-  }
-  return cudaGetLastError();
+cudaError_t launch_chol(const StageArgs& a, const SegTable& seg, bool qr2, cudaStream_t stream) {
+  return qr2 ? launch_small(chol_kernel<true>, a, seg, 2, stream)
+             : launch_small(chol_kernel<false>, a, seg, 1, stream);
 }
 
-cudaError_t launch_eig(const StageArgs& a, const SegTable& seg, int grid, size_t smem,
-                       cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  eig_kernel<<<grid, kSmallWarps * 32, smem, stream>>>(a, seg);
-  return cudaGetLastError();
+cudaError_t launch_eig(const StageArgs& a, const SegTable& seg, cudaStream_t stream) {
+  return launch_small(eig_kernel, a, seg, 1, stream);
 }
 
 }  // namespace staged

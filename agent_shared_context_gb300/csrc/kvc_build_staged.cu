@@ -383,10 +383,11 @@ __device__ __forceinline__ int64_t rows_at(int i, int d, int lp) {
   return static_cast<int64_t>(i) * d * lp;
 }
 
-constexpr int kMRows = 16;       // rows of M per cp.async stage of the M X product
+constexpr int kMRows = 8;        // rows of M per cp.async stage of the M X product (55.5 KB
+                                 // of shared memory at d = 128, l = 40: four CTAs per SM)
 
 // X (Omega, or Z T with T = R^-1 of the previous orthonormalisation), then
-// P1 = M X and G = X^T P1.  M streams through two 16-row stages.
+// P1 = M X and G = X^T P1.  M streams through two kMRows-row stages.
 template <bool kFromZ>
 __global__ void __launch_bounds__(kRowThreads)
     mx_kernel(const StageArgs a, const __grid_constant__ SegTable seg) {
@@ -823,15 +824,12 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 // Every stage over the matrices of each pass.
 cudaError_t run_passes(StageArgs& a, const SegTable& seg, int64_t mats, int64_t NM, int q,
                        const DeviceInfo& di, cudaStream_t stream) {
-  const int d = a.d, lp = a.lp, r = a.r, l = a.l;
+  const int d = a.d, lp = a.lp, r = a.r;
   const size_t gram_smem = 1024 + 2 * 2 * kDP * 128 + 64 + 64;
   const size_t mx_smem = static_cast<size_t>(2 * d * lp + lp * lp + 2 * kMRows * d) * sizeof(float);
   const size_t zg_smem = static_cast<size_t>(lp * lp + 2 * d * lp) * sizeof(float);
   const size_t wp_smem = static_cast<size_t>(2 * lp * lp + lp + 2 * lp * d) * sizeof(float);
   const size_t u_smem = 1024 + 4 * kUAtom + 4 * static_cast<size_t>((r + 15) & ~15) * 128 + 64;
-  const size_t chol_smem = chol_smem_bytes(false, l);
-  const size_t qr2_smem = chol_smem_bytes(true, l);
-  const size_t eig_smem = eig_smem_bytes(l);
   cudaError_t e;
   if ((e = set_smem(gram_kernel, gram_smem)) != cudaSuccess) return e;
   if ((e = set_smem(mx_kernel<false>, mx_smem)) != cudaSuccess) return e;
@@ -845,24 +843,23 @@ cudaError_t run_passes(StageArgs& a, const SegTable& seg, int64_t mats, int64_t 
     const int nm = static_cast<int>(std::min<int64_t>(NM, mats - m0));
     a.m0 = static_cast<int32_t>(m0);
     a.nm = nm;
-    const int sg = (nm + kSmallWarps - 1) / kSmallWarps;
     gram_kernel<<<std::min(nm, gram_slots), kGramThreads, gram_smem, stream>>>(a, seg);
     for (int it = 0; it < q; ++it) {
       if (it == 0)
         mx_kernel<false><<<nm, kRowThreads, mx_smem, stream>>>(a, seg);
       else
         mx_kernel<true><<<nm, kRowThreads, mx_smem, stream>>>(a, seg);
-      if ((e = launch_chol(a, seg, false, sg, chol_smem, stream)) != cudaSuccess) return e;  // R_Y^-1
+      if ((e = launch_chol(a, seg, false, stream)) != cudaSuccess) return e;  // R_Y^-1
       zg_kernel<<<nm, kRowThreads, zg_smem, stream>>>(a, seg);                             // delta^T Q
-      if ((e = launch_chol(a, seg, false, sg, chol_smem, stream)) != cudaSuccess) return e;  // orth
+      if ((e = launch_chol(a, seg, false, stream)) != cudaSuccess) return e;  // orth
     }
     if (q == 0)
       mx_kernel<false><<<nm, kRowThreads, mx_smem, stream>>>(a, seg);
     else
       mx_kernel<true><<<nm, kRowThreads, mx_smem, stream>>>(a, seg);
-    if ((e = launch_chol(a, seg, true, sg, qr2_smem, stream)) != cudaSuccess) return e;     // QR2
+    if ((e = launch_chol(a, seg, true, stream)) != cudaSuccess) return e;     // QR2
     zg_kernel<<<nm, kRowThreads, zg_smem, stream>>>(a, seg);                               // B^T, B B^T
-    if ((e = launch_eig(a, seg, sg, eig_smem, stream)) != cudaSuccess) return e;
+    if ((e = launch_eig(a, seg, stream)) != cudaSuccess) return e;
     wp_kernel<<<nm, kRowThreads, wp_smem, stream>>>(a, seg);
     u_kernel<<<nm, kUThreads, u_smem, stream>>>(a, seg);
     e = cudaGetLastError();

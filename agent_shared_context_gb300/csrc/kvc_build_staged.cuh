@@ -78,14 +78,10 @@ __device__ __forceinline__ const __nv_bfloat16* rows_of(const char* base, const 
 
 // l x l stages (kvc_build_chol.cu), one matrix per warp: qr2 = false writes
 // T = R^-1 of G, qr2 = true the CholeskyQR2 factor R_Y^-1; the eigen stage
-// writes Ub, lam, sigma and eff_rank from G = B B^T.  Shared memory per CTA
-// from the sketch width l.
-cudaError_t launch_chol(const StageArgs& a, const SegTable& seg, bool qr2, int grid, size_t smem,
-                        cudaStream_t stream);
-size_t chol_smem_bytes(bool qr2, int l);
-cudaError_t launch_eig(const StageArgs& a, const SegTable& seg, int grid, size_t smem,
-                       cudaStream_t stream);
-size_t eig_smem_bytes(int l);
+// writes Ub, lam, sigma and eff_rank from G = B B^T.  The launchers size the
+// grid and the shared memory from a.nm and the sketch width a.l.
+cudaError_t launch_chol(const StageArgs& a, const SegTable& seg, bool qr2, cudaStream_t stream);
+cudaError_t launch_eig(const StageArgs& a, const SegTable& seg, cudaStream_t stream);
 
 }  // namespace staged
 }  // namespace kvc
