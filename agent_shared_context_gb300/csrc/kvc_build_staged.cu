@@ -14,10 +14,11 @@
 // steps, each step runs as its own kernel over a pass of up to kPassMats
 // matrices, with the parallelism each step needs:
 //
-//   gram_kernel    delta^T delta on tcgen05 (split bf16 hi + lo, four MMAs per
-//                  16-token step, two shared-memory buffers so the loads and
-//                  conversion of chunk k+1 overlap the MMAs of chunk k); M and
-//                  |delta|_F^2 go to the workspace;
+//   gram_kernel    delta^T delta on tcgen05 (split bf16 hi + lo, three MMAs
+//                  per 16-token step: hi.hi + hi.lo + lo.hi; two shared-
+//                  memory buffers so the loads and conversion of chunk k+1
+//                  overlap the MMAs of chunk k); M and |delta|_F^2 go to the
+//                  workspace;
 //   mx_kernel      (thread = feature row) X (Omega, or Z R^-1 of the previous
 //                  orthonormalisation), P1 = M X, G = X^T P1;
 //   chol_kernel    (warp = matrix) Cholesky with dependent-column dropping and
@@ -175,10 +176,11 @@ __global__ void __launch_bounds__(kGramThreads, 3)
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t dh = desc_kmajor_sw128(hb + ks * 32);
           const uint64_t dl = desc_kmajor_sw128(lb + ks * 32);
+          // hi.hi + hi.lo + lo.hi; the lo.lo term is below 2^-16 of each
+          // product and is left out
           mma_bf16_ss(tmem, dh, dh, kIdescM, (kc | ks) != 0 ? 1u : 0u);
           mma_bf16_ss(tmem, dh, dl, kIdescM, 1u);
           mma_bf16_ss(tmem, dl, dh, kIdescM, 1u);
-          mma_bf16_ss(tmem, dl, dl, kIdescM, 1u);
         }
         mma_commit(&mbar[b]);
       }

@@ -6,7 +6,8 @@ Y^T Y = X^T M X for the implicit CholeskyQR of Y = delta X, delta^T Q =
 M X R_Y^-1 for the next iterate, B^T = delta^T Q for the small SVD, and U =
 delta (X R_Y^-1 Ub_r diag(sigma_r)).  The spans, and so U W^T, equal the
 oracle's in exact arithmetic.  This test replays that sequence in NumPy --
-M accumulated from the hi/lo bf16 split of the delta (RNE), fp32 elsewhere,
+M accumulated from the hi/lo bf16 split of the delta (RNE; hi.hi + hi.lo +
+lo.hi, as the tensor-core Gram forms it), fp32 elsewhere,
 Cholesky with dependent-column dropping -- and requires U W^T within 1e-3 of
 the oracle's (the GPU tolerance is 2e-2 for bf16), on the longctx shape
 (geometric spectrum, bf16 caches) and the noise-free planted tiny delta.
@@ -59,8 +60,9 @@ def _feature_side_state(E1, E0, r, omega, q):
     D = np.asarray(E1, np.float32) - np.asarray(E0, np.float32)
     hi = _bf16(D)
     lo = _bf16(D - hi)
+    # the bf16 kernel's three products (the lo.lo term is left out)
     M = (hi.T.astype(np.float64) @ hi + hi.T.astype(np.float64) @ lo
-         + lo.T.astype(np.float64) @ hi + lo.T.astype(np.float64) @ lo).astype(np.float32)
+         + lo.T.astype(np.float64) @ hi).astype(np.float32)
     X = np.asarray(omega, np.float32)
     for _ in range(q):
         G = X.T @ (M @ X)                               # Y^T Y
