@@ -193,8 +193,9 @@ const char* kvc_last_error(void);
  * aligned); it may be NULL when that size is 0.  bf16 caches (d = 64 or 128)
  * are factored in passes of up to 8,192 matrices (one (segment, layer, head,
  * K|V) block each) and the workspace holds one pass: per matrix the d x d
- * Gram of the delta, the d x l iterates and the l x l factors (about 180 KB
- * at d = 128, l = 40; about 1.5 GB for a full pass).
+ * Gram of the delta, the d x l iterates, the l x l factors and the d x r
+ * factor of U (about 160 KB at d = 128, l = 40, r = 32; about 1.3 GB for a
+ * full pass).
  * ------------------------------------------------------------------------- */
 size_t kvc_build_states_workspace(const kvc_segments* seg, const kvc_params* prm);
 kvc_status kvc_build_states(const kvc_segments* seg, const kvc_params* prm,

@@ -97,7 +97,7 @@ def test_chain_matches_oracle(name):
     2^-9 relative, which moves the mean-pooled query by ~2^-9 / sqrt(3 n)
     per component and a cosine by ~1e-4, and the softmax weights by ~that /
     temperature; weights then get rtol 1e-2 + atol 1e-4 and decisions need a
-    gap of 1e-3 (the survey's decision margin).  Every unit is checked
+    gap of 1e-3 (ten times that cosine shift).  Every unit is checked
     (``check_decisions``).  Outputs follow check_out (its bound grows with
     the edge)."""
     kvc = _kvc()
