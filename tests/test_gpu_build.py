@@ -40,6 +40,10 @@ def _cases():
                                       fallback_frac=0.34),
         "d64-bf16": synth.scaled(LC, L=1, H=2, R=1, seg_len=[300, 64], d=64, A=4, r=24,
                                  oversample=8, fallback_frac=0.0),
+        # sketch width l = 21, not a multiple of 4: the eigen stage's rows are
+        # read in 16-byte chunks over zero padding, the row strides round up
+        "bf16-odd-l": synth.scaled(LC, L=1, H=2, R=1, seg_len=[256, 130], A=4, r=16,
+                                   oversample=5, fallback_frac=0.0),
         # f32 head wider than the tensor-core builder's 128 rows: FP32 builder
         "f32-d256": synth.scaled(tiny, L=1, H=1, R=1, seg_len=[200], d=256),
     }
