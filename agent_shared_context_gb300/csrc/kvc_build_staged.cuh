@@ -12,14 +12,13 @@ namespace staged {
 constexpr int kGramThreads = 256;
 constexpr int kDP = 128;                  // feature rows of the Gram MMA (d padded)
 constexpr int kTok = 64;                  // tokens per delta^T chunk (MMA K)
-constexpr int kLmax = 64;
-constexpr int kSweeps = 14;
-constexpr int kSweepsOneSided = 20;   // bound on one-sided Jacobi sweeps
+constexpr int kLmax = 64;                 // largest sketch width l = r + p
+constexpr int kSweepsOneSided = 20;       // bound on one-sided Jacobi sweeps
 constexpr int kRowThreads = 128;          // feature-row kernels
 constexpr int kSmallWarps = 4;            // l x l kernels: one matrix per warp
 constexpr int kUThreads = 256;
 constexpr int kPassMats = 8192;           // matrices per pass through the stages
-constexpr uint32_t kGramCols = 128;
+constexpr uint32_t kGramCols = 128;       // TMEM columns of the Gram accumulator
 
 struct StageArgs {
   const char* exact[2];
