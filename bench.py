@@ -655,11 +655,16 @@ def _e2e(args, wl, inp, runner, dev):
         assign[i] = k
         load[k] += copies[i][0].numel() * copies[i][0].element_size()
 
+    # The uploads of a step wait only for the previous step's kernels (which
+    # read the inputs), not for its read-back of the outputs, which no upload
+    # touches: the read-back of step k overlaps the uploads of step k + 1 on
+    # the full-duplex link.
+    inputs_free = [None]
+
     def step():
-        ready = torch.cuda.Event()
-        ready.record(stream)                     # the previous step's kernels are done with the inputs
-        for cs in copy_streams:
-            cs.wait_event(ready)
+        if inputs_free[0] is not None:
+            for cs in copy_streams:
+                cs.wait_event(inputs_free[0])
         for i, (h, d) in enumerate(copies):
             with torch.cuda.stream(copy_streams[assign[i]]):
                 d.copy_(h, non_blocking=True)
@@ -668,6 +673,9 @@ def _e2e(args, wl, inp, runner, dev):
             done.record(cs)
             stream.wait_event(done)
         runner.run()
+        ev = torch.cuda.Event()
+        ev.record(stream)                        # this step's kernels are done with the inputs
+        inputs_free[0] = ev
         for h, d in zip(host_out, outs):
             h.copy_(d, non_blocking=True)
 
