@@ -2,10 +2,13 @@
 // (kvc_build_staged.cu), one matrix per warp.
 //
 // A warp keeps its matrices row-major in shared memory, row stride rs.  Lane
-// k owns columns k and k + 32: when the lanes update their own columns of one
-// row they touch consecutive addresses, and a row that all of them need (the
-// pivot row of a Cholesky step, a column of the inverse staged as a vector)
-// is read as 16-byte broadcasts.  The factorisations use an odd row stride,
+// L owns columns l - 1 - L and l - 33 - L: the triangular steps cost a column
+// in proportion to its index, so the first pass over a lane's columns takes
+// the 32 heaviest and the second only the lightest ones.  When the lanes
+// update their own columns of one row they touch consecutive addresses
+// (descending), and a row that all of them need (the pivot row of a Cholesky
+// step, a column of the inverse staged as a vector) is read as 16-byte
+// broadcasts.  The factorisations use an odd row stride,
 // so that lanes walking different rows of one column also hit distinct
 // banks; the eigen stage uses a stride that is a multiple of four with an
 // odd quotient, so that the lanes' 16-byte chunks of different rows fall in
@@ -81,7 +84,7 @@ __device__ __forceinline__ WarpMats warp_mats(float* sh, int warp, int l, int rs
 // the final R[i][i].
 __device__ void chol_rm(float* __restrict__ A, int* keep, float* dinv, float* diag, float* gd,
                         float* __restrict__ vec, int l, int rs, int lane) {
-  for (int k = lane; k < l; k += 32) {
+  for (int k = l - 1 - lane; k >= 0; k -= 32) {
     gd[k] = A[k * rs + k];
     for (int m = k + 1; m < l; ++m) A[m * rs + k] = 0.0f;
   }
@@ -98,8 +101,8 @@ __device__ void chol_rm(float* __restrict__ A, int* keep, float* dinv, float* di
     const int i0 = (j + 1) & ~3;
     for (int i = i0 + lane; i < l; i += 32) vec[i] = i > j ? -A[j * rs + i] * inv2 : 0.0f;
     __syncwarp();
-    for (int k = lane; k < l; k += 32) {
-      if (k <= j) continue;
+    for (int k = l - 1 - lane; k >= 0; k -= 32) {
+      if (k <= j) break;                              // the lane's later columns are smaller
       const float rjk = A[j * rs + k];
       float* ck = A + k;                              // column k, element i at ck[i * rs]
       int i = i0;
@@ -118,7 +121,7 @@ __device__ void chol_rm(float* __restrict__ A, int* keep, float* dinv, float* di
     }
     __syncwarp();
   }
-  for (int k = lane; k < l; k += 32) {
+  for (int k = l - 1 - lane; k >= 0; k -= 32) {
     for (int m = 0; m <= k; ++m) A[m * rs + k] *= dinv[m];
     diag[k] = A[k * rs + k];
   }
@@ -138,8 +141,8 @@ __device__ void tri_inv_rm(float* __restrict__ A, const int* keep, const float* 
     const float inv = keep[i] ? 1.0f / diag[i] : 0.0f;
     for (int m = lane; m < i; m += 32) vec[m] = A[m * rs + i];
     __syncwarp();
-    for (int k = lane; k < l; k += 32) {
-      if (k <= i) continue;
+    for (int k = l - 1 - lane; k >= 0; k -= 32) {
+      if (k <= i) break;                              // the lane's later columns are smaller
       float* ck = A + k;
       const float xi = ck[i * rs] * inv;
       int m = 0;
@@ -160,7 +163,7 @@ __device__ void tri_inv_rm(float* __restrict__ A, const int* keep, const float* 
     if (lane == 0) A[i * rs + i] = keep[i] ? 1.0f : 0.0f;
     __syncwarp();
   }
-  for (int k = lane; k < l; k += 32)
+  for (int k = l - 1 - lane; k >= 0; k -= 32)
     for (int m = 0; m <= k; ++m) A[m * rs + k] *= keep[m] ? 1.0f / diag[m] : 0.0f;
   __syncwarp();
 }
@@ -192,7 +195,7 @@ __device__ void right_mul_upper(float* __restrict__ A, const float* __restrict__
 // H[m][k] = sum_{t <= m} Ri[t][m] H[t][k] (m <= k).
 __device__ void left_mul_upper_t(const float* __restrict__ Ri, float* __restrict__ H, int l,
                                  int rs, int lane) {
-  for (int k = lane; k < l; k += 32) {
+  for (int k = l - 1 - lane; k >= 0; k -= 32) {
     for (int m = k; m >= 0; --m) {
       float acc = 0.0f;
 #pragma unroll 4
