@@ -79,9 +79,9 @@ __device__ __forceinline__ WarpMats warp_mats(float* sh, int warp, int l, int rs
 // dinv at the end; a pivot at or below 1e-6 of its column's original squared
 // norm marks a dependent column (keep[j] = 0, row j zero).  Each step stages
 // its pivot row, scaled by -1 / pivot, in vec from the 4-aligned index below
-// j + 1 (zeros up to j, so those rows are rewritten unchanged), and lane k
-// updates rows of its column k.  gd is scratch for G's diagonal; diag gets
-// the final R[i][i].
+// j + 1 (zeros up to j, so those rows are rewritten unchanged), and each
+// lane updates the rows of its own columns.  gd is scratch for G's diagonal;
+// diag gets the final R[i][i].
 __device__ void chol_rm(float* __restrict__ A, int* keep, float* dinv, float* diag, float* gd,
                         float* __restrict__ vec, int l, int rs, int lane) {
   for (int k = l - 1 - lane; k >= 0; k -= 32) {
@@ -191,7 +191,7 @@ __device__ void right_mul_upper(float* __restrict__ A, const float* __restrict__
 }
 
 // Upper triangle of Ri^T H in place of H: column k of the result depends on
-// column k of H only, so lane k rewrites its columns, rows m descending:
+// column k of H only, so each lane rewrites its own columns, rows m descending:
 // H[m][k] = sum_{t <= m} Ri[t][m] H[t][k] (m <= k).
 __device__ void left_mul_upper_t(const float* __restrict__ Ri, float* __restrict__ H, int l,
                                  int rs, int lane) {
