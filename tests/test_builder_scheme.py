@@ -169,3 +169,60 @@ def test_feature_side_iteration_matches_hmt(case, eig):
         Uo, Wo, _, _ = O.build_unit(E1, E0, r, om, q)
         U, W = _feature_side_state(E1, E0, r, om, q, eig)
         assert O.relative_error(U @ W.T, Uo @ Wo.T) <= 1e-3
+
+
+def _chol_inv_inplace(A):
+    """The l x l stage of the bf16 builder on one float32 array, in its step
+    order: right-looking Cholesky in place (pivot row scaled by -1/pivot,
+    a pivot at or below 1e-6 of its column's original diagonal drops the
+    column), then the in-place back substitution whose step i first updates
+    the columns k > i from column i of R and then turns column i into column
+    i of the inverse.  Returns (R, R^-1, keep)."""
+    f32 = np.float32
+    A = np.array(A, np.float32)
+    l = A.shape[0]
+    gd = np.diag(A).copy()
+    A = np.triu(A)
+    keep = np.zeros(l, bool)
+    dinv = np.zeros(l, np.float32)
+    for j in range(l):
+        piv = A[j, j]
+        ok = gd[j] > 0 and piv > f32(1e-6) * gd[j]
+        inv2 = f32(1) / piv if ok else f32(0)
+        keep[j] = ok
+        dinv[j] = f32(1) / np.sqrt(piv) if ok else f32(0)
+        prow = -A[j, j + 1:] * inv2
+        for k in range(j + 1, l):
+            A[j + 1:k + 1, k] = prow[:k - j] * A[j, k] + A[j + 1:k + 1, k]
+    A = A * dinv[:, None]
+    R = A.copy()
+    diag = np.diag(R).copy()
+    for i in range(l - 1, -1, -1):
+        inv = f32(1) / diag[i] if keep[i] else f32(0)
+        col = A[:i, i].copy()
+        for k in range(i + 1, l):
+            xi = A[i, k] * inv
+            A[:i, k] = -col * xi + A[:i, k]
+        A[:i, i] = -col * inv
+        A[i, i] = f32(1) if keep[i] else f32(0)
+    scale = np.where(keep, f32(1) / np.where(keep, diag, f32(1)), f32(0)).astype(np.float32)
+    return R, np.triu(A) * scale[:, None], keep
+
+
+@pytest.mark.parametrize("l", [8, 21, 40, 64])
+def test_inplace_cholesky_and_inverse(l):
+    """G = R^T R on the kept columns, R^-1 R = I there, dropped indices give
+    zero rows and columns of R^-1, and both factors are upper triangular --
+    on Grams of graded columns with one exactly dependent column."""
+    rng = np.random.default_rng(l)
+    X = rng.standard_normal((200, l)) * np.geomspace(1.0, 1e-2, l)
+    X[:, l // 2] = X[:, l // 2 - 1]                      # a dependent column
+    G = (X.T @ X).astype(np.float32)
+    R, Ri, keep = _chol_inv_inplace(G)
+    assert keep.sum() == l - 1 and not keep[l // 2]
+    kept = np.flatnonzero(keep)
+    Rk = R[np.ix_(kept, kept)].astype(np.float64)
+    assert np.abs(Rk.T @ Rk - G[np.ix_(kept, kept)]).max() <= 1e-5 * np.abs(G).max()
+    assert np.abs(Ri[np.ix_(kept, kept)].astype(np.float64) @ Rk - np.eye(len(kept))).max() <= 1e-3
+    assert np.all(Ri[~keep, :] == 0) and np.all(Ri[:, ~keep] == 0)
+    assert np.all(np.tril(R, -1) == 0) and np.all(np.tril(Ri, -1) == 0)
